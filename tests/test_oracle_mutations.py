@@ -1,0 +1,148 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Every mutation below is a plausible slip (a dropped term, a wrong index, a swapped
+operand, a reversed tie-break). Each is planted into the oracle module on the CPU
+with monkeypatch and the full set of pins from ``test_oracle_pins`` is run: at least
+one pin has to fail, which shows the pins constrain that part of the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import bsattn_oracle as O
+from test_oracle_pins import ALL_CHECKS
+
+
+def _means_divide_by_s(K, T, s):
+    n_sub = -(-T // s)
+    out = np.empty((n_sub, K.shape[1]))
+    for j in range(n_sub):
+        lo, hi = O.sub_block_range(j, s, T)
+        out[j] = np.asarray(K[lo:hi], np.float64).sum(axis=0) / s
+    return out
+
+
+def _scores_no_scale(q, kbar, T, g, s, group_reduce="max"):
+    return ORIG["block_scores"](q, kbar, T, g, s, group_reduce) * math.sqrt(q.shape[1])
+
+
+def _scores_mean_pool(q, kbar, T, g, s, group_reduce="max"):
+    G, d = q.shape
+    n_sub = -(-T // s)
+    sigma = (q @ kbar[:n_sub].T) / math.sqrt(d)
+    r = g // s
+    return np.array([sigma[:, c * r:min((c + 1) * r, n_sub)].mean(axis=1).max()
+                     for c in range(-(-T // g))])
+
+
+def _scores_head0_only(q, kbar, T, g, s, group_reduce="max"):
+    return ORIG["block_scores"](q[:1], kbar, T, g, s, group_reduce)
+
+
+def _topk_high_index(keys, pool, k):
+    return [] if k <= 0 else sorted(pool, key=lambda c: (-float(keys[c]), -c))[:k]
+
+
+def _topk_ascending(keys, pool, k):
+    return [] if k <= 0 else sorted(pool, key=lambda c: (float(keys[c]), c))[:k]
+
+
+def _forced_local_ceil(T, g, sink_tokens, local_tokens):
+    n_blk = -(-T // g)
+    n_sink = min(-(-sink_tokens // g), n_blk)
+    local_lo = -(-max(0, T - local_tokens) // g)
+    return sorted(set(range(n_sink)) | set(range(local_lo, n_blk)))
+
+
+def _forced_sink_floor(T, g, sink_tokens, local_tokens):
+    n_blk = -(-T // g)
+    local_lo = max(0, T - local_tokens) // g
+    return sorted(set(range(min(sink_tokens // g, n_blk))) | set(range(local_lo, n_blk)))
+
+
+def _candidates_with_forced(T, g, sink_tokens, local_tokens):
+    return [c for c in range(-(-T // g)) if (c + 1) * g <= T]
+
+
+def _attention_no_clip(q, K, V, sel, g, T):
+    T2 = min(K.shape[0], max((c + 1) * g for c in sel)) if sel else T
+    return ORIG["sparse_attention"](q, K, V, sel, g, T2)
+
+
+def _attention_values_are_keys(q, K, V, sel, g, T):
+    return ORIG["sparse_attention"](q, K, K, sel, g, T)
+
+
+def _attention_no_scale(q, K, V, sel, g, T):
+    return ORIG["sparse_attention"](q * math.sqrt(q.shape[1]), K, V, sel, g, T)
+
+
+def _attention_lse_no_max(q, K, V, sel, g, T):
+    o, lse = ORIG["sparse_attention"](q, K, V, sel, g, T)
+    U = O.selected_tokens(sel, g, T)
+    m = ((q @ np.asarray(K[U]).T) / math.sqrt(q.shape[1])).max(axis=1)
+    return o, lse - m
+
+
+def _select_no_eviction(cls, T, g, sink_tokens, local_tokens, k, k_e, scores=None, evict=None, alive=None):
+    if cls == O.DUAL and alive is not None:
+        alive = np.ones_like(alive)
+    r = ORIG["select_unit"](cls, T, g, sink_tokens, local_tokens, k, k_e, scores, evict, alive)
+    if r.alive is not None:
+        r.alive[:] = 1
+    return r
+
+
+def _select_gq_overlaps(cls, T, g, sink_tokens, local_tokens, k, k_e, scores=None, evict=None, alive=None):
+    r = ORIG["select_unit"](cls, T, g, sink_tokens, local_tokens, k, k_e, scores, evict, alive)
+    if cls == O.DUAL:
+        C = O.candidate_blocks(T, g, sink_tokens, local_tokens)
+        r.gamma_q = sorted(O.top_k(scores, C, k - k_e))
+        r.sel = sorted(set(O.forced_blocks(T, g, sink_tokens, local_tokens)) | set(r.gamma_e) | set(r.gamma_q))
+    return r
+
+
+def _setdiff_swapped(prev, cur):
+    a, r = ORIG["setdiff"](prev, cur)
+    return r, a
+
+
+def _update_wrong_sub_block(kbar, K, T, s):
+    return ORIG["update_sub_block"](kbar, K, T + 1 if T < K.shape[0] else T, s)
+
+
+MUTATIONS = {
+    "means_divide_by_s": ("sub_block_means", _means_divide_by_s),
+    "scores_no_scale": ("block_scores", _scores_no_scale),
+    "scores_mean_pool": ("block_scores", _scores_mean_pool),
+    "scores_head0_only": ("block_scores", _scores_head0_only),
+    "topk_high_index_ties": ("top_k", _topk_high_index),
+    "topk_ascending": ("top_k", _topk_ascending),
+    "forced_local_ceil": ("forced_blocks", _forced_local_ceil),
+    "forced_sink_floor": ("forced_blocks", _forced_sink_floor),
+    "candidates_with_forced": ("candidate_blocks", _candidates_with_forced),
+    "attention_no_clip": ("sparse_attention", _attention_no_clip),
+    "attention_values_are_keys": ("sparse_attention", _attention_values_are_keys),
+    "attention_no_scale": ("sparse_attention", _attention_no_scale),
+    "attention_lse_no_max": ("sparse_attention", _attention_lse_no_max),
+    "select_no_eviction": ("select_unit", _select_no_eviction),
+    "select_gamma_q_overlaps_gamma_e": ("select_unit", _select_gq_overlaps),
+    "setdiff_swapped": ("setdiff", _setdiff_swapped),
+    "update_wrong_sub_block": ("update_sub_block", _update_wrong_sub_block),
+}
+
+ORIG = {name: getattr(O, name) for name, _ in MUTATIONS.values()}
+
+
+@pytest.mark.parametrize("mutation", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(mutation, monkeypatch):
+    name, fn = MUTATIONS[mutation]
+    monkeypatch.setattr(O, name, fn)
+    failed = []
+    for check in ALL_CHECKS:
+        try:
+            check(O)
+        except Exception as e:  # noqa: BLE001 - any failure of a pin counts
+            failed.append((check.__name__, type(e).__name__))
+    assert failed, f"no pin caught the planted mistake {mutation}"
