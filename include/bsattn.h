@@ -1,0 +1,217 @@
+/*
+ * bsattn.h - block-sparse decode attention over a paged KV cache (C ABI).
+ *
+ * One decode step of one attention layer, for every unit u = (sequence b, KV head
+ * h_kv), u = b * n_kv_heads + h_kv:
+ *
+ *   bs_build_block_summaries  sub-block mean keys kept current as tokens are appended
+ *   bs_score_blocks           block scores: mean-key dot products max-pooled over the
+ *                             sub-blocks of a block and reduced over the GQA group
+ *   bs_select_topk            per-unit block selection: forced sink/local blocks,
+ *                             query-aware top-k, NOSA's eviction-driven dual selection
+ *   bs_sparse_decode_attn     split-KV flash-decode over the selected blocks only
+ *   bs_block_setdiff          blocks added to / removed from the selection since the
+ *                             previous step
+ *
+ * Method sources: "Technisches Resümee: NOSA: Native und Offloadable Sparse
+ * Attention" (section Methodik: "1. Algorithmus: NOSA" and "2. System: NOSI") and
+ * "Technische Samenvatting: Fluxion" (sections Probleemstelling, Kerninzichten,
+ * Systeemcomponenten).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership. The caller allocates and owns every buffer. The library allocates
+ *   nothing and keeps no state between calls; the persistent state of a decode loop
+ *   (summaries, alive mask, previous selection) lives in caller buffers.
+ * Memory spaces. Struct arguments (bs_dims, bs_kv, bs_head_cfg) are HOST structs
+ *   passed by pointer; every array they point to, and every array argument, is
+ *   DEVICE memory unless the parameter says otherwise.
+ * Asynchrony. Each call validates its host-visible arguments, enqueues kernels on
+ *   `stream` and returns. Nothing waits for the GPU.
+ * Errors. Host-detected problems (null pointers, bad shapes, misalignment, a too
+ *   small workspace) return a non-zero bs_status before anything is enqueued.
+ *   A failed launch returns BS_ERR_CUDA. Problems only the device can see (a page
+ *   index outside the pool, a per-unit configuration that breaks a rule below, a
+ *   capacity overflow, a bounded wait that ran out) store the first such code into
+ *   `*dev_status` (an int32 device word the caller zeroes; atomicCAS from 0) and the
+ *   offending unit's work is skipped, never performed out of bounds. Read it after
+ *   synchronising.
+ * Determinism. Results are bitwise reproducible run to run and independent of which
+ *   other units share the batch: no floating-point atomics, and each unit's split
+ *   plan depends only on that unit's own sizes.
+ *
+ * Data layout (dims below are the fields of bs_dims)
+ * ----------------------------------------------------
+ *   K, V pools     [n_pages][page_size=16][head_dim], kv_dtype; 16-byte aligned base.
+ *   page_table     int32 [units][max_pages_per_unit]; entry p of unit u is the
+ *                  physical page holding tokens [16p, 16p+16) of that unit.
+ *   seq_lens       int32 [batch]; T = tokens in the cache including the current
+ *                  decode token, which sits at position T-1.
+ *   q              [batch][n_q_heads][head_dim], q_dtype; query heads
+ *                  [h_kv*G, (h_kv+1)*G) share KV head h_kv (G = n_q_heads/n_kv_heads).
+ *   summaries      float32; unit u's sub-block j occupies
+ *                  summaries[sum_off[u] + j*head_dim ... + head_dim).
+ *   scores         float32 [units][max_blocks_per_unit].
+ *   evict_logits   float32 [units][max_blocks_per_unit] (dual units only).
+ *   alive          uint8   [units][max_blocks_per_unit] (dual units only; start at 1).
+ *   sel_idx        int32   [units][max_sel_per_unit], ascending, padded with -1.
+ *   sel_cnt        int32   [units].
+ *   out            float32 [batch][n_q_heads][head_dim];  lse float32 [batch][n_q_heads].
+ */
+#ifndef BSATTN_H_
+#define BSATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. NULL selects the legacy default stream. */
+typedef struct CUstream_st *bs_stream_t;
+
+typedef enum {
+  BS_OK = 0,
+  BS_ERR_INVALID_ARG = 1,   /* null pointer, value out of its documented range */
+  BS_ERR_SHAPE = 2,         /* unsupported head_dim, group size or page size */
+  BS_ERR_ALIGN = 3,         /* a pointer or offset breaks its alignment rule */
+  BS_ERR_CAPACITY = 4,      /* a buffer or row is too small for the data */
+  BS_ERR_CUDA = 5,          /* a CUDA launch failed */
+  BS_ERR_DEVICE_BOUNDS = 6, /* (device) a page index outside the pool or table */
+  BS_ERR_TIMEOUT = 7        /* (device) a bounded wait ran out */
+} bs_status;
+
+typedef enum { BS_BF16 = 0, BS_FP32 = 1 } bs_dtype;
+
+/* Head classes (Fluxion, Kerninzichten item 2: streaming vs retrieval heads;
+ * NOSA, Dual-Selection-Mechanismus: query-aware plus query-agnostic selection). */
+typedef enum { BS_STREAMING = 0, BS_RETRIEVAL = 1, BS_DUAL = 2 } bs_head_class;
+
+/* How the G query heads of a group combine their max-pooled block scores
+ * (Fluxion, Systeemcomponenten: GQA handled at group level). */
+typedef enum { BS_GROUP_MAX = 0, BS_GROUP_MEAN = 1 } bs_group_reduce;
+
+/* Shapes and capacities, host struct. Supported: head_dim 64 or 128, page_size 16,
+ * G = n_q_heads / n_kv_heads in 1..8, max_blocks_per_unit <= 16384. */
+typedef struct {
+  int32_t batch, n_q_heads, n_kv_heads, head_dim, page_size;
+  int32_t max_pages_per_unit;        /* page-table row length */
+  int32_t max_blocks_per_unit;       /* row length of scores / evict_logits / alive */
+  int32_t max_sel_per_unit;          /* row length of sel_idx and of setdiff outputs */
+  int32_t max_subs_per_unit;         /* upper bound on ceil(T/s) over units (grid sizing) */
+  int32_t max_gather_pages_per_unit; /* upper bound on pages covered by a selection */
+  int64_t n_pages;                   /* pages in each of the K and V pools */
+  bs_dtype kv_dtype, q_dtype;
+} bs_dims;
+
+/* Paged KV cache: device pointers. */
+typedef struct {
+  const void *k_pool, *v_pool;
+  const int32_t *page_table;
+  const int32_t *seq_lens;
+} bs_kv;
+
+/* Per-unit head properties, struct of arrays of length batch * n_kv_heads, device
+ * memory (host memory for bs_check_head_cfg only). These are the outputs of the
+ * pages' head-property predictor and granularity-budget selector, taken as inputs.
+ * Rules (checked by bs_check_head_cfg on the host and by every kernel on the device):
+ *   cls in {STREAMING, RETRIEVAL, DUAL};  g % 16 == 0;  g % s == 0 and g/s a power
+ *   of two <= 64;  k >= 0;  0 <= k_e <= k (k_e used by DUAL units only);
+ *   sink_tokens >= 0;  local_tokens >= 1 (the current token is always attended);
+ *   sum_off % 4 == 0 (16-byte aligned summary rows); sum_rows >= ceil(T/s).
+ * Selection: forced blocks F = [0, ceil(sink/g)) U [floor(max(0,T-local)/g), ceil(T/g));
+ * candidates C = complete blocks outside F; streaming: S = F; retrieval: S = F plus
+ * the k best of C; dual: S = F plus Gamma_e (k_e best alive blocks of C by eviction
+ * logit) plus Gamma_q (k - k_e best of C minus Gamma_e by score). Ties go to the
+ * lower block index. */
+typedef struct {
+  const int32_t *cls, *block_tokens, *sub_tokens, *k_total, *k_evict;
+  const int32_t *sink_tokens, *local_tokens;
+  const int64_t *sum_off;   /* float offset of unit u's first summary row */
+  const int32_t *sum_rows;  /* summary rows reserved for unit u */
+} bs_head_cfg;
+
+/* Host-side check of a head configuration whose nine arrays are in HOST memory.
+ * `seq_lens_host` (length batch) are the largest lengths the caller will use.
+ * Returns BS_OK or the first rule broken (BS_ERR_INVALID_ARG, BS_ERR_ALIGN,
+ * BS_ERR_CAPACITY). Launches nothing. */
+bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *cfg_host,
+                            const int32_t *seq_lens_host);
+
+/* a1. Sub-block key summaries.
+ * NOSA, "Blockweise Implementierung": mean pooling inside sub-blocks is the first
+ * stage of the two-stage pooling; NOSI fuses the pooling with the KV write.
+ * For each unit of sequence b, recomputes every sub-block j that holds a token of
+ * [tok_begin[b], seq_lens[b]): kbar_j = (1/n_j) sum of K[t] over the n_j tokens of
+ * [j*s, min((j+1)*s, T)), summed in token order in fp32. A decode step passes
+ * tok_begin = T-1 (one sub-block per unit); a prefill passes 0. The result does not
+ * depend on how the range was split across calls.
+ * tok_begin: device int32 [batch]. max_new_tokens (host): an upper bound on
+ * seq_lens[b] - tok_begin[b], used only to size the grid. */
+bs_status bs_build_block_summaries(const bs_dims *dims, const bs_kv *kv, const bs_head_cfg *cfg,
+                                   const int32_t *tok_begin, int32_t max_new_tokens,
+                                   float *summaries, int32_t *dev_status, bs_stream_t stream);
+
+/* a2. Block scores.
+ * NOSA, "Blockweise Implementierung": max pooling at block level over the sub-block
+ * means; Fluxion, "Granularity-Budget Selector": one selection per GQA group.
+ * For every retrieval or dual unit and every candidate block c:
+ *   S[c] = reduce_{h in group} max_{j in sub-blocks of c} (q_h . kbar_j) / sqrt(d),
+ * reduce = max (BS_GROUP_MAX) or mean (BS_GROUP_MEAN). Entries of the row outside
+ * the candidate range are written as -inf; rows of streaming units are not touched. */
+bs_status bs_score_blocks(const bs_dims *dims, const void *q, const bs_head_cfg *cfg,
+                          const int32_t *seq_lens, const float *summaries,
+                          bs_group_reduce group_reduce, float *scores, int32_t *dev_status,
+                          bs_stream_t stream);
+
+/* a3. Block selection.
+ * Fluxion, Kerninzichten item 2 (streaming vs retrieval heads, per-head budget and
+ * granularity); NOSA, Dual-Selection-Mechanismus (Gamma_q, Gamma_e and the strict
+ * eviction rule: a block of C that is not in Gamma_e is marked dead in `alive` and
+ * never enters Gamma_e again) and ED-DMA (selection on pre-exponential logits).
+ * Writes S of every unit, ascending, into sel_idx (padded with -1) and |S| into
+ * sel_cnt. evict_logits and alive may be NULL when no unit is DUAL (a DUAL unit
+ * with NULL arrays reports BS_ERR_INVALID_ARG on the device). Scores and logits are
+ * compared exactly as float32 order keys. */
+bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int32_t *seq_lens,
+                         const float *scores, const float *evict_logits, uint8_t *alive,
+                         int32_t *sel_idx, int32_t *sel_cnt, int32_t *dev_status,
+                         bs_stream_t stream);
+
+/* a4. Sparse decode attention.
+ * Fluxion, Probleemstelling item 1 (sparse attention over the selected KV blocks)
+ * and Kerninzichten item 3 (bound by data movement). For each query head h of unit
+ * u, over the tokens U of the selected blocks (each clipped to t < T):
+ *   out_h = sum_t softmax_t(q_h . K[t] / sqrt(d)) V[t],  lse_h = log sum_t exp(q_h . K[t] / sqrt(d)).
+ * Split-KV: a unit's gathered pages are cut into at most 32 contiguous splits whose
+ * size depends only on that unit's page count; each split keeps an fp32 online
+ * softmax and the partials are merged by log-sum-exp.
+ * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
+ * aligned; its contents need no initialisation and are overwritten. */
+bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
+                                const bs_head_cfg *cfg, const int32_t *sel_idx,
+                                const int32_t *sel_cnt, float *out, float *lse, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_status, bs_stream_t stream);
+
+/* a5. Set-difference of selections.
+ * NOSA, "2. System: NOSI": set-difference kernels drive block swapping.
+ * added = cur \ prev and removed = prev \ cur per unit, both ascending, padded with
+ * -1 to max_sel_per_unit; counts in added_cnt / removed_cnt. prev_cnt[u] = 0 gives
+ * added = cur (first step). Input lists must be ascending and duplicate-free. */
+bs_status bs_block_setdiff(const bs_dims *dims, const int32_t *prev_idx, const int32_t *prev_cnt,
+                           const int32_t *cur_idx, const int32_t *cur_cnt, int32_t *added,
+                           int32_t *added_cnt, int32_t *removed, int32_t *removed_cnt,
+                           int32_t *dev_status, bs_stream_t stream);
+
+/* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
+size_t bs_workspace_size(const bs_dims *dims);
+
+/* Static text for a status code. */
+const char *bs_status_string(bs_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSATTN_H_ */

@@ -1,0 +1,88 @@
+// Host-side parts of the C ABI that launch nothing: status text, shape checks,
+// head-configuration checks and workspace sizing.
+#include <cstdint>
+
+#include "bs_attn_plan.cuh"
+#include "bs_internal.cuh"
+
+namespace bsi {
+
+bs_status check_dims(const bs_dims *d) {
+  if (d == nullptr) return BS_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->n_kv_heads < 1 || d->n_q_heads < 1) return BS_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads != 0) return BS_ERR_SHAPE;
+  const int G = d->n_q_heads / d->n_kv_heads;
+  if (G > kMaxG) return BS_ERR_SHAPE;
+  if (d->head_dim != 64 && d->head_dim != 128) return BS_ERR_SHAPE;
+  if (d->page_size != kPage) return BS_ERR_SHAPE;
+  if (d->kv_dtype != BS_BF16 && d->kv_dtype != BS_FP32) return BS_ERR_INVALID_ARG;
+  if (d->q_dtype != BS_BF16 && d->q_dtype != BS_FP32) return BS_ERR_INVALID_ARG;
+  if (d->max_pages_per_unit < 1 || d->max_blocks_per_unit < 1 || d->max_sel_per_unit < 1 ||
+      d->max_subs_per_unit < 1 || d->max_gather_pages_per_unit < 1 || d->n_pages < 1)
+    return BS_ERR_INVALID_ARG;
+  if (d->max_blocks_per_unit > kMaxBlocks) return BS_ERR_CAPACITY;
+  if (static_cast<int64_t>(d->batch) * d->n_kv_heads > (int64_t(1) << 24)) return BS_ERR_CAPACITY;
+  return BS_OK;
+}
+
+}  // namespace bsi
+
+extern "C" {
+
+const char *bs_status_string(bs_status s) {
+  switch (s) {
+    case BS_OK: return "ok";
+    case BS_ERR_INVALID_ARG: return "invalid argument";
+    case BS_ERR_SHAPE: return "unsupported shape";
+    case BS_ERR_ALIGN: return "misaligned pointer or offset";
+    case BS_ERR_CAPACITY: return "capacity exceeded";
+    case BS_ERR_CUDA: return "CUDA launch failed";
+    case BS_ERR_DEVICE_BOUNDS: return "device index out of bounds";
+    case BS_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t bs_workspace_size(const bs_dims *dims) {
+  if (bsi::check_dims(dims) != BS_OK) return 0;
+  const int G = dims->n_q_heads / dims->n_kv_heads;
+  const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
+  return units * bsi::kAttnMaxSplits * G * bsi::attn_record_floats(dims->head_dim) * sizeof(float);
+}
+
+bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *c, const int32_t *seq_lens_host) {
+  bs_status st = bsi::check_dims(dims);
+  if (st != BS_OK) return st;
+  if (c == nullptr || seq_lens_host == nullptr) return BS_ERR_INVALID_ARG;
+  if (!c->cls || !c->block_tokens || !c->sub_tokens || !c->k_total || !c->k_evict || !c->sink_tokens ||
+      !c->local_tokens || !c->sum_off || !c->sum_rows)
+    return BS_ERR_INVALID_ARG;
+  for (int b = 0; b < dims->batch; ++b) {
+    const int T = seq_lens_host[b];
+    if (T < 1) return BS_ERR_INVALID_ARG;
+    if ((T + bsi::kPage - 1) / bsi::kPage > dims->max_pages_per_unit) return BS_ERR_CAPACITY;
+    for (int h = 0; h < dims->n_kv_heads; ++h) {
+      const int u = b * dims->n_kv_heads + h;
+      const int g = c->block_tokens[u], s = c->sub_tokens[u];
+      if (!bsi::unit_cfg_ok(c->cls[u], g, s, c->k_total[u], c->k_evict[u], c->sink_tokens[u],
+                            c->local_tokens[u]))
+        return BS_ERR_INVALID_ARG;
+      if (c->sum_off[u] < 0) return BS_ERR_INVALID_ARG;
+      if (c->sum_off[u] % 4 != 0) return BS_ERR_ALIGN;
+      const int n_sub = (T + s - 1) / s, n_blk = (T + g - 1) / g;
+      if (n_sub > c->sum_rows[u] || n_sub > dims->max_subs_per_unit) return BS_ERR_CAPACITY;
+      if (n_blk > dims->max_blocks_per_unit) return BS_ERR_CAPACITY;
+      const bsi::Geom ge = bsi::unit_geom(T, g, s, c->sink_tokens[u], c->local_tokens[u]);
+      const int forced = ge.n_sink + (ge.n_blk - (ge.local_lo > ge.n_sink ? ge.local_lo : ge.n_sink));
+      int sel = forced + (c->cls[u] == BS_STREAMING ? 0 : c->k_total[u]);
+      if (sel > ge.n_blk) sel = ge.n_blk;
+      if (sel > dims->max_sel_per_unit) return BS_ERR_CAPACITY;
+      if (static_cast<int64_t>(sel) * (g / bsi::kPage) >
+          dims->max_gather_pages_per_unit)
+        return BS_ERR_CAPACITY;
+    }
+  }
+  return BS_OK;
+}
+
+}  // extern "C"

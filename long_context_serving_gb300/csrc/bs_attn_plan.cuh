@@ -1,0 +1,43 @@
+// Split-KV plan of bs_sparse_decode_attn, shared by the split kernel, the merge
+// kernel and the workspace size.
+#pragma once
+
+#include "bs_internal.cuh"
+
+namespace bsi {
+
+constexpr int kAttnThreads = 256;                  // 8 warps
+constexpr int kStagePages = 4;                     // pages staged per pipeline step
+constexpr int kStageTokens = kStagePages * kPage;  // 64 tokens
+constexpr int kAttnMaxSplits = 32;                 // splits per unit, at most
+
+// One partial record per (unit, split, head): o[D] (unnormalised), m (log2 units), l, 2 pad.
+__host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
+
+// Pages covered by a unit's selection: every selected block but the last is complete
+// (only the tail block can be partial and it has the largest index).
+struct UnitPages {
+  int n_pages;   // gathered pages (0 when the unit has nothing to attend or is invalid)
+  int ppb;       // pages per block
+  int pps;       // pages per split (a multiple of kStagePages)
+  int n_split;
+};
+
+__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk) {
+  UnitPages p;
+  p.ppb = g / kPage;
+  p.n_pages = 0;
+  p.pps = kStagePages;
+  p.n_split = 0;
+  if (cnt <= 0 || T < 1 || last_blk < 0 || last_blk * g >= T) return p;
+  const int rem_pages = (T - last_blk * g + kPage - 1) / kPage;
+  const int last_pages = rem_pages < p.ppb ? rem_pages : p.ppb;
+  p.n_pages = (cnt - 1) * p.ppb + last_pages;
+  int per = (p.n_pages + kStagePages * kAttnMaxSplits - 1) / (kStagePages * kAttnMaxSplits);
+  if (per < 1) per = 1;
+  p.pps = kStagePages * per;
+  p.n_split = (p.n_pages + p.pps - 1) / p.pps;
+  return p;
+}
+
+}  // namespace bsi

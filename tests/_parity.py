@@ -1,0 +1,134 @@
+"""Step-by-step parity of the CUDA path against the float64 oracle.
+
+Tolerances (floating point; integer outputs are compared exactly):
+* attention output: max-abs 2e-3 and max-rel 1e-2, the relative error taken against
+  max(|ref|, 0.2) so that near-zero references fall under the absolute bound;
+  lse: max-abs 2e-3;
+* sub-block means: fp32 sums of at most s bf16 values (|x| <= ~30 with planted
+  needles and sink): |err| <= s * 2^-24 * sum|x| well under 1e-4 absolute;
+* block scores: fp32 dot products of 128 terms: |err| <= 128 * 2^-24 *
+  ||q|| ||kbar|| / sqrt(d), at most ~2e-4 for the planted needles; 3e-4 absolute
+  plus 1e-5 relative is allowed.
+Selections and set-differences must match exactly wherever the oracle's k-th and
+(k+1)-th keys are not a near-tie; at a near-tie the oracle's selection is fed to the
+GPU attention and set-difference so that both sides keep the same state.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from long_context_serving_gb300 import bsattn as B
+from long_context_serving_gb300.layer import PagedLayer
+from oracle import bsattn_oracle as O
+
+ATT_ABS, ATT_REL, REL_FLOOR = 2e-3, 1e-2, 0.2
+LSE_ABS = 2e-3
+SUM_ABS = 1e-4
+SCORE_ABS, SCORE_REL = 3e-4, 1e-5
+
+
+@dataclass
+class Report:
+    att_abs: float = 0.0
+    att_rel: float = 0.0
+    lse_abs: float = 0.0
+    sum_abs: float = 0.0
+    score_abs: float = 0.0
+    compared_units: int = 0
+    near_ties: int = 0
+    exact_selections: int = 0
+    notes: list = field(default_factory=list)
+
+    def check(self):
+        assert self.att_abs <= ATT_ABS, self
+        assert self.att_rel <= ATT_REL, self
+        assert self.lse_abs <= LSE_ABS, self
+        assert self.sum_abs <= SUM_ABS, self
+        assert self.score_abs <= SCORE_ABS, self
+        assert self.compared_units > 0
+
+
+def attention_errors(o_gpu: np.ndarray, o_ref: np.ndarray):
+    diff = np.abs(o_gpu.astype(np.float64) - o_ref)
+    return float(diff.max()), float((diff / np.maximum(np.abs(o_ref), REL_FLOOR)).max())
+
+
+def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_sample=None, seed=0) -> Report:
+    """Drive the GPU path and the oracle through the same steps on ``units`` (default all)."""
+    units = list(range(wl.U)) if units is None else list(units)
+    reduce_code = B.BS_GROUP_MAX if group_reduce == "max" else B.BS_GROUP_MEAN
+    rng = np.random.default_rng(seed)
+    layer = PagedLayer(wl)
+    layer.prefill()
+    state = O.init_state(wl, units)
+    rep = Report()
+    G = wl.G
+    for step in range(wl.steps if steps is None else steps):
+        layer.append(step)
+        layer.update_summaries(step)
+        layer.score(step, reduce_code)
+        layer.select(step)
+        torch.cuda.synchronize()
+        res = O.decode_step(wl, step, state, units, group_reduce)
+        gsel = layer.selection(layer.cur)
+        scores = layer.scores.cpu().numpy()
+        alive = layer.alive.cpu().numpy() if layer.alive is not None else None
+        override = {}
+        for u in units:
+            r = res[u]
+            g, s = int(wl.g[u]), int(wl.s[u])
+            n_sub = -(-r.T // s)
+            # a1: summaries (the updated row plus every row or a sample)
+            rows = np.arange(n_sub) if summary_rows_sample is None else np.unique(
+                np.concatenate([[n_sub - 1], rng.integers(0, n_sub, size=min(summary_rows_sample, n_sub))]))
+            gs = layer.unit_summaries(u, n_sub)
+            rep.sum_abs = max(rep.sum_abs, float(np.abs(gs[rows] - state[u].kbar[rows]).max()))
+            if wl.cls[u] != O.STREAMING:
+                # a2: scores on candidates, -inf elsewhere
+                C = O.candidate_blocks(r.T, g, int(wl.sink[u]), int(wl.local[u]))
+                if C:
+                    err = np.abs(scores[u, C] - r.scores[C]) - SCORE_REL * np.abs(r.scores[C])
+                    rep.score_abs = max(rep.score_abs, float(err.max()))
+                mask = np.ones(layer.max_blocks, bool)
+                mask[C] = False
+                assert np.all(scores[u, mask] == -np.inf), (step, u)
+            # a3: selection
+            if r.sel.near_tie:
+                rep.near_ties += 1
+                if gsel[u] != r.sel.sel:
+                    override[u] = r.sel.sel
+            else:
+                assert gsel[u] == r.sel.sel, (step, u, gsel[u], r.sel.sel)
+                rep.exact_selections += 1
+            if wl.cls[u] == O.DUAL:
+                n_blk = -(-r.T // g)
+                assert np.array_equal(alive[u, :n_blk], r.sel.alive[:n_blk]), (step, u)
+        if override:
+            layer.set_selection(override)
+        layer.attend(step)
+        layer.setdiff()
+        torch.cuda.synchronize()
+        out = layer.out.cpu().numpy()
+        lse = layer.lse.cpu().numpy()
+        added = layer.added.cpu().numpy()
+        added_cnt = layer.added_cnt.cpu().numpy()
+        removed = layer.removed.cpu().numpy()
+        removed_cnt = layer.removed_cnt.cpu().numpy()
+        for u in units:
+            r = res[u]
+            b, hk = divmod(u, wl.Hkv)
+            a_abs, a_rel = attention_errors(out[b, hk * G:(hk + 1) * G], r.o)
+            rep.att_abs, rep.att_rel = max(rep.att_abs, a_abs), max(rep.att_rel, a_rel)
+            rep.lse_abs = max(rep.lse_abs, float(np.abs(lse[b, hk * G:(hk + 1) * G] - r.lse).max()))
+            assert added[u, :added_cnt[u]].tolist() == r.added, (step, u)
+            assert removed[u, :removed_cnt[u]].tolist() == r.removed, (step, u)
+            assert (added[u, added_cnt[u]:] == -1).all() and (removed[u, removed_cnt[u]:] == -1).all()
+            rep.compared_units += 1
+        layer.advance()
+        status = layer.read_status()
+        assert status == 0, f"device status {status}: {B.status_string(status)}"
+    return rep

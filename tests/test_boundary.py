@@ -1,0 +1,126 @@
+"""The C-ABI library on the host: it loads, exports what include/bsattn.h declares, and
+rejects bad arguments with the documented status before launching anything. Nothing
+here touches a GPU: every call below returns during host-side validation."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from long_context_serving_gb300 import bsattn as B
+from long_context_serving_gb300.build import build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    return B.lib()
+
+
+def test_exports_every_declared_function():
+    names = B.header_functions()
+    assert {"bs_build_block_summaries", "bs_score_blocks", "bs_select_topk", "bs_sparse_decode_attn",
+            "bs_block_setdiff", "bs_workspace_size", "bs_status_string", "bs_check_head_cfg"} <= set(names)
+    for n in names:
+        assert hasattr(B.lib(), n), n
+
+
+def test_status_strings():
+    for code in range(8):
+        assert B.status_string(code) not in ("", "unknown status")
+    assert B.status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, page_size=16, max_pages_per_unit=64,
+                max_blocks_per_unit=32, max_sel_per_unit=16, max_subs_per_unit=128, max_gather_pages_per_unit=32,
+                n_pages=128, kv_dtype=B.BS_BF16, q_dtype=B.BS_BF16)
+    base.update(kw)
+    return B.Dims(**base)
+
+
+def test_workspace_size():
+    d = _dims()
+    ws = B.workspace_size(d)
+    assert ws > 0 and ws % 16 == 0
+    assert B.workspace_size(_dims(batch=4)) == 2 * ws
+    for bad in (dict(head_dim=96), dict(page_size=32), dict(n_q_heads=9), dict(n_q_heads=18),
+                dict(batch=0), dict(max_blocks_per_unit=20000), dict(kv_dtype=7)):
+        assert B.workspace_size(_dims(**bad)) == 0, bad
+
+
+class HostCfg:
+    """Head configuration in host memory for bs_check_head_cfg."""
+
+    def __init__(self, U, **kw):
+        vals = dict(cls=B.BS_RETRIEVAL, block_tokens=32, sub_tokens=8, k_total=4, k_evict=0, sink_tokens=32,
+                    local_tokens=32, sum_off=None, sum_rows=128)
+        vals.update(kw)
+        self.arrays = {}
+        for k, v in vals.items():
+            dt = np.int64 if k == "sum_off" else np.int32
+            if k == "sum_off" and v is None:
+                v = np.arange(U, dtype=np.int64) * 128 * 128
+            self.arrays[k] = np.ascontiguousarray(np.broadcast_to(np.asarray(v, dtype=dt), (U,)))
+        self.cfg = B.HeadCfg(**{k: a.ctypes.data for k, a in self.arrays.items()})
+
+
+def _check(dims, U=4, T=1000, **kw):
+    hc = HostCfg(U, **kw)
+    lens = np.full(dims.batch, T, np.int32)
+    return B.check_head_cfg(dims, hc.cfg, lens)
+
+
+def test_check_head_cfg_rules():
+    d = _dims()
+    assert _check(d) == B.BS_OK
+    assert _check(d, block_tokens=24) == B.BS_ERR_INVALID_ARG          # g % 16
+    assert _check(d, sub_tokens=5) == B.BS_ERR_INVALID_ARG             # g % s
+    assert _check(d, block_tokens=96, sub_tokens=32) == B.BS_ERR_INVALID_ARG   # g/s = 3
+    assert _check(d, block_tokens=1024, sub_tokens=8) == B.BS_ERR_INVALID_ARG  # g/s > 64
+    assert _check(d, local_tokens=0) == B.BS_ERR_INVALID_ARG
+    assert _check(d, k_total=-1) == B.BS_ERR_INVALID_ARG
+    assert _check(d, cls=B.BS_DUAL, k_total=4, k_evict=5) == B.BS_ERR_INVALID_ARG
+    assert _check(d, cls=3) == B.BS_ERR_INVALID_ARG
+    assert _check(d, sum_off=np.array([0, 6, 12, 18])) == B.BS_ERR_ALIGN
+    assert _check(d, sum_rows=100) == B.BS_ERR_CAPACITY                # ceil(1000/8) = 125 rows
+    assert _check(d, k_total=20) == B.BS_ERR_CAPACITY                  # more than max_sel
+    assert _check(d, T=2000) == B.BS_ERR_CAPACITY                      # more pages than the table row
+    assert _check(d, T=0) == B.BS_ERR_INVALID_ARG
+    assert B.check_head_cfg(d, HostCfg(4).cfg, None) == B.BS_ERR_INVALID_ARG
+
+
+def test_calls_reject_bad_arguments_before_launch():
+    L = B.lib()
+    d = _dims()
+    kv = B.KV(k_pool=0x10000, v_pool=0x20000, page_table=0x30000, seq_lens=0x40000)
+    cfg = B.HeadCfg(*([0x50000] * 9))
+    st = ctypes.c_void_p(0x60000)
+    ref = ctypes.byref
+    # null pointers
+    assert L.bs_build_block_summaries(ref(d), ref(kv), ref(cfg), None, 1, 0x70000, st, None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_score_blocks(ref(d), None, ref(cfg), 0x1000, 0x2000, 0, 0x3000, st, None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_select_topk(ref(d), ref(cfg), None, 0x1000, None, None, 0x2000, 0x3000, st, None) == \
+        B.BS_ERR_INVALID_ARG
+    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, None,
+                                   1 << 30, st, None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_block_setdiff(ref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, st,
+                              None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_score_blocks(None, 0x1000, ref(cfg), 0x1000, 0x2000, 0, 0x3000, st, None) == B.BS_ERR_INVALID_ARG
+    # bad shapes
+    assert L.bs_score_blocks(ref(_dims(head_dim=80)), 0x1000, ref(cfg), 0x1000, 0x2000, 0, 0x3000, st, None) == \
+        B.BS_ERR_SHAPE
+    assert L.bs_select_topk(ref(_dims(n_q_heads=20)), ref(cfg), 0x1000, 0x1000, None, None, 0x2000, 0x3000, st,
+                            None) == B.BS_ERR_SHAPE
+    # misaligned pointers
+    assert L.bs_sparse_decode_attn(ref(d), 0x1002, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+                                   1 << 30, st, None) == B.BS_ERR_ALIGN
+    bad_kv = B.KV(k_pool=0x10008, v_pool=0x20000, page_table=0x30000, seq_lens=0x40000)
+    assert L.bs_build_block_summaries(ref(d), ref(bad_kv), ref(cfg), 0x1000, 1, 0x70000, st, None) == B.BS_ERR_ALIGN
+    assert L.bs_score_blocks(ref(d), 0x1000, ref(cfg), 0x1000, 0x2004, 0, 0x3000, st, None) == B.BS_ERR_ALIGN
+    # invalid values
+    assert L.bs_score_blocks(ref(d), 0x1000, ref(cfg), 0x1000, 0x2000, 5, 0x3000, st, None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_build_block_summaries(ref(d), ref(kv), ref(cfg), 0x1000, 0, 0x70000, st, None) == \
+        B.BS_ERR_INVALID_ARG
+    # workspace too small
+    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+                                   16, st, None) == B.BS_ERR_CAPACITY

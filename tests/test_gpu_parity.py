@@ -1,0 +1,197 @@
+"""GPU parity of the five calls against the float64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+from _parity import run_parity
+from long_context_serving_gb300 import bsattn as B
+from long_context_serving_gb300.build import build
+from long_context_serving_gb300.layer import PagedLayer
+from oracle import bsattn_oracle as O
+from workloads import make_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build()
+    B.lib()
+
+
+# Shrunken versions of the five configurations: several tiles, ragged tails, and the
+# multi-step ones cross a block boundary during the run.
+SMALL = {
+    "cfg1-tiny": (1, {}),
+    "cfg2-T4133": (2, dict(T=4096 + 37)),
+    "cfg3-B2-T9210x12": (3, dict(B=2, T=9210, steps=12)),
+    "cfg4-B3-T3000..6000": (4, dict(B=3, T_range=(3000, 6000))),
+    "cfg5-B4-T2040x16": (5, dict(B=4, T=2040, steps=16)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_parity_small(name):
+    cfg, kw = SMALL[name]
+    rep = run_parity(make_workload(cfg, seed=1, **kw))
+    rep.check()
+
+
+def test_parity_group_mean():
+    rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
+    rep.check()
+
+
+# Full sizes of the configurations, with outputs sampled on a subset of units.
+def _sample_units(wl, n):
+    rng = np.random.default_rng(7)
+    by_cls = {c: [u for u in range(wl.U) if wl.cls[u] == c] for c in (O.STREAMING, O.RETRIEVAL, O.DUAL)}
+    pick = []
+    for c, us in by_cls.items():
+        if us:
+            pick += rng.choice(us, size=min(len(us), max(1, n // 2)), replace=False).tolist()
+    return sorted(set(pick))[:max(n, 2)]
+
+
+@pytest.mark.parametrize("cfg,n_units", [(1, None), (2, None), (3, 6), (4, 6), (5, 6)])
+def test_parity_full_size(cfg, n_units):
+    wl = make_workload(cfg, seed=0)
+    units = None if n_units is None else _sample_units(wl, n_units)
+    rep = run_parity(wl, units, summary_rows_sample=None if cfg <= 2 else 256)
+    rep.check()
+
+
+def test_batch_invariance():
+    """A sub-batch gives bitwise the same outputs as the full batch."""
+    outs = []
+    for Bn in (3, 2):
+        layer = PagedLayer(make_workload(4, seed=5, B=Bn, T_range=(3000, 6000)))
+        layer.prefill()
+        layer.append(0)
+        layer.step(0)
+        torch.cuda.synchronize()
+        outs.append((layer.out.cpu(), layer.lse.cpu(), layer.selection(1 - layer.cur)))
+        assert layer.read_status() == 0
+    (o3, l3, s3), (o2, l2, s2) = outs
+    assert torch.equal(o3[:2], o2) and torch.equal(l3[:2], l2)
+    assert s3[:2 * 4] == s2
+
+
+def test_incremental_summaries_equal_rebuild_bitwise():
+    wl = make_workload(3, seed=3, B=1, T=5000, steps=40)
+    layer = PagedLayer(wl)
+    layer.prefill()
+    for step in range(wl.steps):
+        layer.append(step)
+        layer.update_summaries(step)
+    inc = layer.summaries.clone()
+    layer.summaries.fill_(float("nan"))
+    last = layer.seq_lens[wl.steps - 1].clone()
+    B.build_block_summaries(layer.dims, layer.kv_at(last), layer.cfg, layer.zeros_b, int(last.max()),
+                            layer.summaries, layer.status)
+    torch.cuda.synchronize()
+    for u in range(wl.U):
+        rows = -(-int(last[0]) // int(wl.s[u]))
+        off = int(layer._cfg_host["sum_off"][u])
+        a = inc[off:off + rows * wl.d]
+        bb = layer.summaries[off:off + rows * wl.d]
+        assert torch.equal(a, bb), u
+    assert layer.read_status() == 0
+
+
+def test_select_exact_on_crafted_ties():
+    """Scores with many exact ties: the GPU top-k equals the oracle's (lowest index wins)."""
+    wl = make_workload(2, seed=4, T=6000)
+    layer = PagedLayer(wl)
+    rng = np.random.default_rng(0)
+    T = int(wl.T(0, 0))
+    for trial in range(6):
+        vals = rng.integers(-3, 4, size=layer.scores.shape).astype(np.float32)
+        if trial == 0:
+            vals[:] = 1.0
+        if trial == 1:
+            vals[:] = -0.0
+        layer.scores.copy_(torch.from_numpy(vals))
+        layer.select(0)
+        torch.cuda.synchronize()
+        got = layer.selection(layer.cur)
+        for u in range(wl.U):
+            ref = O.select_unit(int(wl.cls[u]), T, int(wl.g[u]), int(wl.sink[u]), int(wl.local[u]),
+                                int(wl.k[u]), 0, vals[u].astype(np.float64))
+            assert got[u] == ref.sel, (trial, u)
+    assert layer.read_status() == 0
+
+
+def test_dual_select_exact_on_crafted_ties():
+    """Dual selection over steps with tied logits and scores: exact Gamma_e/Gamma_q and alive."""
+    wl = make_workload(5, seed=6, B=2, T=1000, steps=40)
+    wl.evict = np.round(wl.evict * 2).astype(np.float32) / 2          # ties in eviction logits
+    layer = PagedLayer(wl)
+    rng = np.random.default_rng(1)
+    alive_ref = {u: np.ones(layer.max_blocks, np.uint8) for u in range(wl.U)}
+    for step in range(wl.steps):
+        vals = rng.integers(-2, 3, size=layer.scores.shape).astype(np.float32)
+        layer.scores.copy_(torch.from_numpy(vals))
+        layer.select(step)
+        torch.cuda.synchronize()
+        got = layer.selection(layer.cur)
+        alive = layer.alive.cpu().numpy()
+        for u in range(wl.U):
+            T = wl.T(step, u // wl.Hkv)
+            ref = O.select_unit(O.DUAL, T, int(wl.g[u]), int(wl.sink[u]), int(wl.local[u]), int(wl.k[u]),
+                                int(wl.k_e[u]), vals[u].astype(np.float64), wl_evict_row(wl, u, layer.max_blocks),
+                                alive_ref[u])
+            alive_ref[u] = ref.alive
+            assert got[u] == ref.sel, (step, u)
+            assert np.array_equal(alive[u], ref.alive), (step, u)
+        layer.advance()
+    assert layer.read_status() == 0
+
+
+def wl_evict_row(wl, u, n):
+    row = np.full(n, -np.inf)
+    row[:min(n, wl.evict.shape[1])] = wl.evict[u, :n]
+    return row
+
+
+def test_setdiff_random_lists():
+    wl = make_workload(2, seed=8, T=3000)
+    layer = PagedLayer(wl)
+    rng = np.random.default_rng(2)
+    MS = layer.max_sel
+    prev, cur = {}, {}
+    for u in range(wl.U):
+        prev[u] = sorted(rng.choice(200, size=int(rng.integers(0, MS + 1)), replace=False).tolist())
+        cur[u] = sorted(rng.choice(200, size=int(rng.integers(0, MS + 1)), replace=False).tolist())
+    layer.set_selection(prev, which=1 - layer.cur)
+    layer.set_selection(cur, which=layer.cur)
+    layer.setdiff()
+    torch.cuda.synchronize()
+    a, ac = layer.added.cpu().numpy(), layer.added_cnt.cpu().numpy()
+    r, rc = layer.removed.cpu().numpy(), layer.removed_cnt.cpu().numpy()
+    for u in range(wl.U):
+        ra, rr = O.setdiff(prev[u], cur[u])
+        assert a[u, :ac[u]].tolist() == ra and r[u, :rc[u]].tolist() == rr
+    assert layer.read_status() == 0
+
+
+def test_out_of_range_page_reports_and_skips():
+    """A page-table entry outside the pool sets BS_ERR_DEVICE_BOUNDS; nothing faults."""
+    wl = make_workload(2, seed=9, T=3000)
+    layer = PagedLayer(wl, preload_all=True)
+    layer.prefill()
+    torch.cuda.synchronize()
+    assert layer.read_status() == 0
+    layer.page_table[4, 0] = wl.n_pages + 5        # sink page of a retrieval unit
+    layer.page_table[0, 3] = -7                    # a sink page of a streaming unit
+    layer.step(0)
+    torch.cuda.synchronize()
+    assert layer.read_status() == B.BS_ERR_DEVICE_BOUNDS
+    # the context is still usable
+    layer.page_table.copy_(torch.from_numpy(wl.page_table))
+    layer.status.zero_()
+    layer.step(0)
+    torch.cuda.synchronize()
+    assert layer.read_status() == 0
