@@ -187,8 +187,14 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * Split-KV: a unit's gathered pages are cut into at most 32 contiguous splits whose
  * size depends only on that unit's page count; each split keeps an fp32 online
  * softmax and the partials are merged by log-sum-exp.
+ * The last split of a unit to finish (an int32 arrival counter per unit) merges the
+ * unit's partials in split order, so the result does not depend on timing.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
- * aligned; its contents need no initialisation and are overwritten. */
+ * aligned. It starts with one int32 arrival counter per unit (padded to 16 bytes);
+ * these must be zero before the first call: zero the workspace once after
+ * allocating it. Every call that completes leaves them zero again; after a call
+ * that reported BS_ERR_TIMEOUT, zero them again. The rest is overwritten per call.
+ * Calls that share a workspace must not run concurrently. */
 bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
                                 const bs_head_cfg *cfg, const int32_t *sel_idx,
                                 const int32_t *sel_cnt, float *out, float *lse, void *workspace,

@@ -15,7 +15,10 @@
 //   * P.V: warp w takes tokens w, w+8, ...; lane l owns head_dim/32 dimensions and
 //     accumulates all G heads;
 //   * the 8 warps' accumulators are summed through shared memory and the split writes
-//     its (o, m, l) record. A second kernel merges a unit's records by log-sum-exp.
+//     its (o, m, l) record to the workspace;
+//   * the last split of a unit to finish (an integer arrival ticket per unit) merges
+//     the unit's records in split order by log-sum-exp and writes out and lse. A unit
+//     with a single split writes its output directly.
 // Tokens past T inside a partial tail page are masked out of both products.
 #include <math.h>
 
@@ -90,7 +93,7 @@ struct AttnLayout {
   static_assert(2 * kStageBytes >= 8 * G * D * 4, "reduction scratch must fit in the K stages");
 };
 
-// Validated per-unit view shared by the split and merge kernels.
+// Validated per-unit view: selection size, gathered pages and split plan.
 struct UnitView {
   bool ok;
   int T, g, cnt;
@@ -128,7 +131,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(bs_dims dims, 
                                                                   bs_kv kv, bs_head_cfg cfg,
                                                                   const int32_t *__restrict__ sel_idx,
                                                                   const int32_t *__restrict__ sel_cnt,
-                                                                  float *__restrict__ ws, int32_t *st) {
+                                                                  int32_t *__restrict__ arrivals,
+                                                                  float *__restrict__ ws, float *__restrict__ out,
+                                                                  float *__restrict__ lse, int32_t *st) {
   using L = AttnLayout<D, KT, G>;
   constexpr int DPL = D / 32;
   constexpr int EPC = KvTraits<KT>::kElemsPerChunk;
@@ -141,8 +146,19 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(bs_dims dims, 
   const int u = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const UnitView uv = unit_view(dims, kv, cfg, sel_idx, sel_cnt, u, st, split == 0 && tid == 0);
-  if (!uv.ok || split >= uv.pg.n_split) return;
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
+  constexpr int QD = D / 4;
+  const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
+  if (!uv.ok) {
+    // Nothing to attend (or an invalid unit): zero output, lse = -inf.
+    if (split == 0)
+      for (int i = tid; i < G * QD; i += kAttnThreads) {
+        reinterpret_cast<float4 *>(out + (orow0 + i / QD) * D)[i % QD] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i % QD == 0) lse[orow0 + i / QD] = -INFINITY;
+      }
+    return;
+  }
+  if (split >= uv.pg.n_split) return;
   const int ppb = uv.pg.ppb;
   const int gp0 = split * uv.pg.pps;
   const int gp1 = min(gp0 + uv.pg.pps, uv.pg.n_pages);
@@ -310,70 +326,86 @@ __global__ void __launch_bounds__(kAttnThreads) attn_split_kernel(bs_dims dims, 
     if (warp == 0 && it + 2 < n_stages) issue(it + 2, buf);
   }
 
-  // ---- sum the 8 warps' accumulators; write this split's record -------------
+  // ---- sum the 8 warps' accumulators ------------------------------------------
   float *red = reinterpret_cast<float *>(smem);  // [8][G][D] over the K stages
 #pragma unroll
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int j = 0; j < DPL; ++j) red[(warp * G + h) * D + lane * DPL + j] = acc[h][j];
+  __shared__ float ml_sm[2][kMaxG];
+  if (warp < G && lane == 0) {
+    ml_sm[0][warp] = m_run;
+    ml_sm[1][warp] = l_run;
+  }
   __syncthreads();
   constexpr int REC = attn_record_floats(D);
-  float *rec = ws + (static_cast<size_t>(u) * kAttnMaxSplits + split) * G * REC;
-  for (int i = tid; i < G * D; i += kAttnThreads) {
-    const int h = i / D, dd = i - h * D;
-    float sum = 0.0f;
+  if (uv.pg.n_split == 1) {
+    // Single split: normalise and write the output directly.
+    for (int i = tid; i < G * QD; i += kAttnThreads) {
+      const int h = i / QD, dq = i % QD;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int w = 0; w < 8; ++w) sum += red[(w * G + h) * D + dd];
-    rec[h * REC + dd] = sum;
-  }
-  if (warp < G && lane == 0) {
-    rec[warp * REC + D] = m_run;
-    rec[warp * REC + D + 1] = l_run;
-  }
-}
-
-// Merge a unit's split records: M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum 2^(m_i - M) o_i / L, lse = ln 2 (M + log2 L).
-template <int D, int G>
-__global__ void attn_merge_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg, const int32_t *__restrict__ sel_idx,
-                                  const int32_t *__restrict__ sel_cnt, const float *__restrict__ ws,
-                                  float *__restrict__ out, float *__restrict__ lse, int32_t *st) {
-  constexpr int QD = D / 4;
-  constexpr int REC = attn_record_floats(D);
-  const int u = blockIdx.x;
-  const int h = threadIdx.x / QD, dq = threadIdx.x % QD;
-  if (h >= G) return;
-  const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
-  const size_t orow = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G + h;
-  const UnitView uv = unit_view(dims, kv, cfg, sel_idx, sel_cnt, u, st, false);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!uv.ok) {
-    reinterpret_cast<float4 *>(out + orow * D)[dq] = o;
-    if (dq == 0) lse[orow] = -INFINITY;
+      for (int w = 0; w < 8; ++w) {
+        const float4 r = reinterpret_cast<const float4 *>(red + (w * G + h) * D)[dq];
+        o.x += r.x; o.y += r.y; o.z += r.z; o.w += r.w;
+      }
+      const float inv = 1.0f / ml_sm[1][h];
+      o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+      reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+      if (dq == 0) lse[orow0 + h] = (ml_sm[0][h] + log2f(ml_sm[1][h])) * kLn2;
+    }
     return;
   }
-  const float *base = ws + static_cast<size_t>(u) * kAttnMaxSplits * G * REC + h * REC;
-  float M = -INFINITY;
-  for (int i = 0; i < uv.pg.n_split; ++i) M = fmaxf(M, base[static_cast<size_t>(i) * G * REC + D]);
-  float Lsum = 0.0f;
-  for (int i = 0; i < uv.pg.n_split; ++i) {
-    const float *r = base + static_cast<size_t>(i) * G * REC;
-    const float mi = r[D];
-    const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - M);
-    Lsum = fmaf(r[D + 1], w, Lsum);
-    const float4 oi = reinterpret_cast<const float4 *>(r)[dq];
-    o.x = fmaf(oi.x, w, o.x);
-    o.y = fmaf(oi.y, w, o.y);
-    o.z = fmaf(oi.z, w, o.z);
-    o.w = fmaf(oi.w, w, o.w);
+  float *rec = ws + (static_cast<size_t>(u) * kAttnMaxSplits + split) * G * REC;
+  for (int i = tid; i < G * QD; i += kAttnThreads) {
+    const int h = i / QD, dq = i % QD;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      const float4 r = reinterpret_cast<const float4 *>(red + (w * G + h) * D)[dq];
+      o.x += r.x; o.y += r.y; o.z += r.z; o.w += r.w;
+    }
+    reinterpret_cast<float4 *>(rec + h * REC)[dq] = o;
   }
-  const float inv = 1.0f / Lsum;
-  o.x *= inv;
-  o.y *= inv;
-  o.z *= inv;
-  o.w *= inv;
-  reinterpret_cast<float4 *>(out + orow * D)[dq] = o;
-  if (dq == 0) lse[orow] = (M + log2f(Lsum)) * kLn2;
+  if (tid < G) {
+    rec[tid * REC + D] = ml_sm[0][tid];
+    rec[tid * REC + D + 1] = ml_sm[1][tid];
+  }
+  // Publish the record, then take an arrival ticket; the last split merges.
+  __threadfence();
+  __syncthreads();
+  __shared__ int is_last;
+  if (tid == 0) is_last = (atomicAdd(arrivals + u, 1) == uv.pg.n_split - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // Merge: M = max m_i, L = sum l_i 2^(m_i - M), o = sum 2^(m_i - M) o_i / L,
+  // lse = ln 2 (M + log2 L); splits are visited in index order.
+  const float *base = ws + static_cast<size_t>(u) * kAttnMaxSplits * G * REC;
+  for (int i = tid; i < G * QD; i += kAttnThreads) {
+    const int h = i / QD, dq = i % QD;
+    const float *hb = base + h * REC;
+    float M = -INFINITY;
+    for (int sp = 0; sp < uv.pg.n_split; ++sp) M = fmaxf(M, __ldcg(hb + static_cast<size_t>(sp) * G * REC + D));
+    float Lsum = 0.0f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < uv.pg.n_split; ++sp) {
+      const float *r = hb + static_cast<size_t>(sp) * G * REC;
+      const float mi = __ldcg(r + D);
+      const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - M);
+      Lsum = fmaf(__ldcg(r + D + 1), w, Lsum);
+      const float4 oi = __ldcg(reinterpret_cast<const float4 *>(r) + dq);
+      o.x = fmaf(oi.x, w, o.x);
+      o.y = fmaf(oi.y, w, o.y);
+      o.z = fmaf(oi.z, w, o.z);
+      o.w = fmaf(oi.w, w, o.w);
+    }
+    const float inv = 1.0f / Lsum;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+    if (dq == 0) lse[orow0 + h] = (M + log2f(Lsum)) * kLn2;
+  }
+  if (tid == 0) arrivals[u] = 0;  // ready for the next call
 }
 
 template <int D, typename KT, int G>
@@ -388,11 +420,10 @@ bs_status launch_attn(const bs_dims &dims, const void *q, const bs_kv &kv, const
   int splits = (dims.max_gather_pages_per_unit + kStagePages - 1) / kStagePages;
   if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
   if (splits < 1) splits = 1;
-  attn_split_kernel<D, KT, G><<<dim3(splits, units), kAttnThreads, L::kBytes, cs>>>(dims, q, kv, cfg, sel_idx,
-                                                                                    sel_cnt, ws, st);
-  if (cudaGetLastError() != cudaSuccess) return BS_ERR_CUDA;
-  constexpr int threads = ((G * D / 4) + 31) / 32 * 32;
-  attn_merge_kernel<D, G><<<units, threads, 0, cs>>>(dims, kv, cfg, sel_idx, sel_cnt, ws, out, lse, st);
+  int32_t *arrivals = reinterpret_cast<int32_t *>(ws);
+  float *records = ws + attn_counter_floats(units);
+  attn_split_kernel<D, KT, G><<<dim3(splits, units), kAttnThreads, L::kBytes, cs>>>(
+      dims, q, kv, cfg, sel_idx, sel_cnt, arrivals, records, out, lse, st);
   return launch_status();
 }
 

@@ -14,6 +14,9 @@ constexpr int kAttnMaxSplits = 32;                 // splits per unit, at most
 // One partial record per (unit, split, head): o[D] (unnormalised), m (log2 units), l, 2 pad.
 __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 
+// The workspace starts with one int32 arrival counter per unit, padded to 16 bytes.
+__host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (units + 3) / 4 * 4; }
+
 // Pages covered by a unit's selection: every selected block but the last is complete
 // (only the tail block can be partial and it has the largest index).
 struct UnitPages {

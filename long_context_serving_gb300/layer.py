@@ -116,7 +116,7 @@ class PagedLayer:
         self.removed_cnt = torch.zeros(U, dtype=torch.int32, device=dev)
         self.out = torch.zeros((wl.B, wl.Hq, d), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((wl.B, wl.Hq), dtype=torch.float32, device=dev)
-        self.workspace = torch.empty(max(B.workspace_size(self.dims) // 4, 4), dtype=torch.float32, device=dev)
+        self.workspace = torch.zeros(max(B.workspace_size(self.dims) // 4, 4), dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     # -- caller-side KV writes (not a step of the method) --------------------------
