@@ -200,6 +200,28 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
                                 const int32_t *sel_cnt, float *out, float *lse, void *workspace,
                                 size_t workspace_bytes, int32_t *dev_status, bs_stream_t stream);
 
+/* a4, without a workspace argument. The pages have no counterpart of this call; it
+ * exists for callers that cannot allocate device memory for a workspace: a plugin
+ * inside a host engine that owns every allocation and offers no allocator, or a
+ * serving loop that may not call cudaMalloc once it runs (the call synchronises the
+ * device and can fail under memory pressure). Same inputs, outputs and results as
+ * bs_sparse_decode_attn, but the split partials and arrival counters live in a fixed
+ * 8 MiB array inside this library's device memory, which every GPU that loads the
+ * library keeps until the process exits.
+ * Limit: bs_workspace_size(dims) must not exceed 8 MiB (for head_dim 128 and G = 4
+ * that is 62 units); larger dims return BS_ERR_CAPACITY before anything is enqueued.
+ * The first call on each device looks up the array's device address with that device
+ * current and caches it; make that first call before any stream capture.
+ * Every call clears the arrival counters on `stream` before its kernel. All calls
+ * share the one array per device, so calls whose kernels overlap on the GPU (on
+ * different streams, or from different threads) race and corrupt each other's
+ * results; serialise them. Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine. */
+bs_status bs_sparse_decode_attn_noalloc(const bs_dims *dims, const void *q, const bs_kv *kv,
+                                        const bs_head_cfg *cfg, const int32_t *sel_idx,
+                                        const int32_t *sel_cnt, float *out, float *lse,
+                                        int32_t *dev_status, bs_stream_t stream);
+
 /* a5. Set-difference of selections.
  * NOSA, "2. System: NOSI": set-difference kernels drive block swapping.
  * added = cur \ prev and removed = prev \ cur per unit, both ascending, padded with

@@ -73,6 +73,9 @@ _SIGS = {
     "bs_block_setdiff": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "bs_sparse_decode_attn_noalloc": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, _P(KV), _P(HeadCfg),
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -165,6 +168,15 @@ def block_setdiff(dims, prev_idx, prev_cnt, cur_idx, cur_cnt, added, added_cnt, 
            lib().bs_block_setdiff(ctypes.byref(dims), _ptr(prev_idx), _ptr(prev_cnt), _ptr(cur_idx), _ptr(cur_cnt),
                                   _ptr(added), _ptr(added_cnt), _ptr(removed), _ptr(removed_cnt), _ptr(dev_status),
                                   _stream(stream)))
+
+
+def sparse_decode_attn_noalloc(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, dev_status, stream=None):
+    """bs_sparse_decode_attn for callers that cannot allocate a workspace: the library's
+    fixed per-device scratch array stands in for it (see include/bsattn.h)."""
+    _check("bs_sparse_decode_attn_noalloc",
+           lib().bs_sparse_decode_attn_noalloc(ctypes.byref(dims), _ptr(q), ctypes.byref(kv), ctypes.byref(cfg),
+                                               _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse),
+                                               _ptr(dev_status), _stream(stream)))
 
 
 def workspace_size(dims) -> int:

@@ -472,3 +472,77 @@ extern "C" bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, c
     return dispatch_g<64, uint16_t>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
   return dispatch_g<64, float>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
 }
+
+// ---------------------------------------------------------------------------
+// Attention without a caller-provided workspace.
+//
+// Some callers cannot hand this library a workspace: a plugin running inside a host
+// engine that owns every device allocation and exposes no allocator, or a serving
+// loop that forbids cudaMalloc after start-up because it synchronises the device and
+// can fail under memory pressure. For them the split records and arrival counters
+// live in a fixed array in this library's own device memory. Each GPU that loads the
+// library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace bsi {
+namespace {
+
+constexpr size_t kFixedScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_fixed_scratch_mu;
+void *g_fixed_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_fixed_scratch on the current device. In host code the array's
+// name only stands in for the symbol; the address is looked up once per device (with
+// that device current) and cached.
+bs_status fixed_scratch_address(void **addr) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_fixed_scratch_mu);
+  if (g_fixed_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fixed_scratch) != cudaSuccess || p == nullptr) return BS_ERR_CUDA;
+    g_fixed_scratch_addr[dev] = p;
+  }
+  *addr = g_fixed_scratch_addr[dev];
+  return BS_OK;
+}
+
+}  // namespace
+}  // namespace bsi
+
+extern "C" bs_status bs_sparse_decode_attn_noalloc(const bs_dims *dims, const void *q, const bs_kv *kv,
+                                                   const bs_head_cfg *cfg, const int32_t *sel_idx,
+                                                   const int32_t *sel_cnt, float *out, float *lse,
+                                                   int32_t *dev_status, bs_stream_t stream) {
+  using namespace bsi;
+  bs_status s = check_dims(dims);
+  if (s != BS_OK) return s;
+  if (!q || !kv || !cfg || !kv->k_pool || !kv->v_pool || !kv->page_table || !kv->seq_lens || !cfg->block_tokens ||
+      !sel_idx || !sel_cnt || !out || !lse || !dev_status)
+    return BS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv->k_pool) || !aligned16(kv->v_pool) || !aligned16(out)) return BS_ERR_ALIGN;
+  const size_t need = bs_workspace_size(dims);
+  if (need > kFixedScratchBytes) return BS_ERR_CAPACITY;
+  void *scratch = nullptr;
+  s = fixed_scratch_address(&scratch);
+  if (s != BS_OK) return s;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  // The arrival counters must start at zero; the array keeps whatever the previous
+  // call (possibly one that stopped early) left in it.
+  const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
+  if (cudaMemsetAsync(scratch, 0, attn_counter_floats(units) * sizeof(float), cs) != cudaSuccess) return BS_ERR_CUDA;
+  const int G = dims->n_q_heads / dims->n_kv_heads;
+  float *ws = static_cast<float *>(scratch);
+  if (dims->head_dim == 128) {
+    if (dims->kv_dtype == BS_BF16)
+      return dispatch_g<128, uint16_t>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
+    return dispatch_g<128, float>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
+  }
+  if (dims->kv_dtype == BS_BF16)
+    return dispatch_g<64, uint16_t>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
+  return dispatch_g<64, float>(G, *dims, q, *kv, *cfg, sel_idx, sel_cnt, out, lse, ws, dev_status, cs);
+}
