@@ -9,7 +9,8 @@ its own cache, summaries and selection buffers (about 0.5 GB touched per step, w
 above the 129 MB L2, so no layer's data is cache-resident when its turn comes). Per
 layer: sub-block update, block scores, selection, sparse attention, set-difference.
 The 32 layers are captured in CUDA graphs (one per parity of the previous/current
-selection buffers) and replayed.
+selection buffers) and replayed. By default each layer is one bs_decode_step call (two
+launches); --path calls uses the five separate calls instead.
 
 Reported: microseconds per layer per decode step (lower is better), the roofline
 of the dominant kernel against HBM bandwidth, an end-to-end figure through pinned
@@ -255,11 +256,14 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
 
     def layer_calls(layer):
-        layer.update_summaries(0)
-        layer.score(0)
-        layer.select(0)
-        layer.attend(0)
-        layer.setdiff()
+        if args.path == "fused":
+            B.decode_step(layer.dims, layer.kv_at(layer.seq_lens[0]), layer.cfg, layer.step_io(0))
+        else:
+            layer.update_summaries(0)
+            layer.score(0)
+            layer.select(0)
+            layer.attend(0)
+            layer.setdiff()
 
     # Eager warm-up of both buffer parities (also the first selection / set-difference).
     for parity in (0, 1):
@@ -279,7 +283,7 @@ def run_ours(args) -> None:
             for layer in layers:
                 layer_calls(layer)
         graphs.append(g)
-    launches_per_step = 5 * LAYERS
+    launches_per_step = (2 if args.path == "fused" else 5) * LAYERS
 
     def timed_replays(graph_list, n):
         stream = torch.cuda.current_stream()
@@ -348,7 +352,8 @@ def run_ours(args) -> None:
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel_name,
                 "peak_source": peak_note, "algorithmic_bytes_per_launch": nbytes[dominant],
-                "launch_us": round(per_kernel[dominant], 3)}
+                "launch_us": round(per_kernel[dominant], 3),
+                "timed_as": "graph of this call over the 32 layers, us per launch"}
 
     # End to end: every step copies q for all layers from pinned host memory, replays,
     # and reads back out, lse and the set-difference lists into pinned host memory.
@@ -391,14 +396,17 @@ def run_ours(args) -> None:
         line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": _config({"ranks": world, "parallelism": f"replicas x{world}, units independent"}),
+                "config": _config({"ranks": world, "parallelism": f"replicas x{world}, units independent",
+                                   "path": args.path,
+                                   "graph": f"CUDA graph of 32 layers x {launches_per_step // LAYERS} launches"}),
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "kernels_us_per_launch": {k: round(v, 3) for k, v in per_kernel.items()},
                 "algorithmic_bytes_per_layer": nbytes,
-                "layer_step_gbs": round(nbytes["layer_step"] / (value * 1e-6) / 1e9, 1)}
+                "layer_step_gbs": round(nbytes["layer_step"] / (value * 1e-6) / 1e9, 1),
+                "layer_step_frac": round(nbytes["layer_step"] / (value * 1e-6) / 1e9 / peak, 4)}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -412,6 +420,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-reps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["fused", "calls"], default="fused",
+                    help="fused: bs_decode_step per layer; calls: the five separate calls per layer")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layer buffers per step (fewer only for profiling small cases)")
     args = ap.parse_args()

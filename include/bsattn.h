@@ -12,6 +12,7 @@
  *   bs_sparse_decode_attn     split-KV flash-decode over the selected blocks only
  *   bs_block_setdiff          blocks added to / removed from the selection since the
  *                             previous step
+ *   bs_decode_step            all five for one layer in two launches
  *
  * Method sources: "Technisches Resümee: NOSA: Native und Offloadable Sparse
  * Attention" (section Methodik: "1. Algorithmus: NOSA" and "2. System: NOSI") and
@@ -190,7 +191,7 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * The last split of a unit to finish (an int32 arrival counter per unit) merges the
  * unit's partials in split order, so the result does not depend on timing.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
- * aligned. It starts with one int32 arrival counter per unit (padded to 16 bytes);
+ * aligned. It starts with two int32 arrival counters per unit (padded to 16 bytes);
  * these must be zero before the first call: zero the workspace once after
  * allocating it. Every call that completes leaves them zero again; after a call
  * that reported BS_ERR_TIMEOUT, zero them again. The rest is overwritten per call.
@@ -231,6 +232,41 @@ bs_status bs_block_setdiff(const bs_dims *dims, const int32_t *prev_idx, const i
                            const int32_t *cur_idx, const int32_t *cur_cnt, int32_t *added,
                            int32_t *added_cnt, int32_t *removed, int32_t *removed_cnt,
                            int32_t *dev_status, bs_stream_t stream);
+
+/* Buffers of one decode step of one layer for bs_decode_step (device pointers). */
+typedef struct {
+  const void *q;              /* [batch][n_q_heads][head_dim], q_dtype */
+  float *summaries;           /* as for bs_build_block_summaries; the sub-block holding T-1 is rewritten */
+  float *scores;              /* [units][max_blocks_per_unit] scratch: this step's candidate scores */
+  const float *evict_logits;  /* [units][max_blocks_per_unit]; may be NULL when no unit is DUAL */
+  uint8_t *alive;             /* [units][max_blocks_per_unit], in/out; may be NULL when no unit is DUAL */
+  const int32_t *prev_idx, *prev_cnt;  /* previous step's selection (prev_cnt 0 at the first step) */
+  int32_t *cur_idx, *cur_cnt;          /* this step's selection (written); must not alias prev */
+  int32_t *added, *added_cnt, *removed, *removed_cnt;  /* set-difference (written) */
+  float *out, *lse;           /* attention output (written) */
+  void *workspace;            /* as for bs_sparse_decode_attn: bs_workspace_size bytes, counters zeroed once */
+  size_t workspace_bytes;
+  int32_t *dev_status;
+} bs_step_io;
+
+/* One decode step of one layer: a1, a2, a3, a4 and a5 in two launches.
+ * The results are those of bs_score_blocks, bs_select_topk, bs_sparse_decode_attn and
+ * bs_block_setdiff called in that order, plus the a1 update of the one sub-block that
+ * holds token T-1 (call bs_build_block_summaries first if more than one token was
+ * appended since the last step). Only the order of fp32 additions inside the
+ * attention may differ from the separate calls (streaming units split their pages
+ * differently), which stays within rounding.
+ * Launch 1 scores every candidate tile; the last tile of each unit selects, writes
+ * the selection and set-difference and updates a1 (that sub-block lies in the forced
+ * tail block, which no score of this step reads). Launch 2 is the attention, launched
+ * as a programmatic dependent: streaming units' splits start before launch 1 ends.
+ * Both launches may begin before the work ahead of them in `stream` has finished;
+ * before waiting for it they read only the per-unit head configuration (cfg arrays),
+ * so those must not be written by the kernel immediately before this call. Everything
+ * else is read after that work has finished. Requires max_sel_per_unit <= 4096.
+ * Errors as for the separate calls; after BS_ERR_TIMEOUT zero the workspace again. */
+bs_status bs_decode_step(const bs_dims *dims, const bs_kv *kv, const bs_head_cfg *cfg, const bs_step_io *io,
+                         bs_group_reduce group_reduce, bs_stream_t stream);
 
 /* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
 size_t bs_workspace_size(const bs_dims *dims);

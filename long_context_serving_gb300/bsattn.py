@@ -51,6 +51,16 @@ class HeadCfg(ctypes.Structure):
                 ("local_tokens", ctypes.c_void_p), ("sum_off", ctypes.c_void_p), ("sum_rows", ctypes.c_void_p)]
 
 
+class StepIO(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("summaries", ctypes.c_void_p), ("scores", ctypes.c_void_p),
+                ("evict_logits", ctypes.c_void_p), ("alive", ctypes.c_void_p), ("prev_idx", ctypes.c_void_p),
+                ("prev_cnt", ctypes.c_void_p), ("cur_idx", ctypes.c_void_p), ("cur_cnt", ctypes.c_void_p),
+                ("added", ctypes.c_void_p), ("added_cnt", ctypes.c_void_p), ("removed", ctypes.c_void_p),
+                ("removed_cnt", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("dev_status", ctypes.c_void_p)]
+
+
 class BsError(RuntimeError):
     def __init__(self, call: str, status: int, text: str):
         super().__init__(f"{call} returned {status} ({text})")
@@ -76,6 +86,7 @@ _SIGS = {
     "bs_sparse_decode_attn_noalloc": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, _P(KV), _P(HeadCfg),
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "bs_decode_step": (ctypes.c_int, [_P(Dims), _P(KV), _P(HeadCfg), _P(StepIO), ctypes.c_int, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -177,6 +188,12 @@ def sparse_decode_attn_noalloc(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, dev
            lib().bs_sparse_decode_attn_noalloc(ctypes.byref(dims), _ptr(q), ctypes.byref(kv), ctypes.byref(cfg),
                                                _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse),
                                                _ptr(dev_status), _stream(stream)))
+
+
+def decode_step(dims, kv, cfg, io: StepIO, group_reduce=BS_GROUP_MAX, stream=None):
+    """All five steps of one layer's decode step (two launches)."""
+    _check("bs_decode_step", lib().bs_decode_step(ctypes.byref(dims), ctypes.byref(kv), ctypes.byref(cfg),
+                                                  ctypes.byref(io), int(group_reduce), _stream(stream)))
 
 
 def workspace_size(dims) -> int:

@@ -25,6 +25,44 @@ bs_status check_dims(const bs_dims *d) {
   return BS_OK;
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+}  // namespace
+
+bs_status make_kv_tensor_maps(const bs_dims &d, const bs_kv &kv, CUtensorMap *tk, CUtensorMap *tv) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return BS_ERR_CUDA;
+  const uint64_t rows = static_cast<uint64_t>(d.n_pages) * kPage;
+  if (rows > (uint64_t(1) << 32)) return BS_ERR_CAPACITY;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim), rows};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
+  const cuuint32_t estr[2] = {1, 1};
+  for (int i = 0; i < 2; ++i) {
+    void *base = const_cast<void *>(i == 0 ? kv.k_pool : kv.v_pool);
+    CUresult r = enc(i == 0 ? tk : tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return BS_ERR_CUDA;
+  }
+  return BS_OK;
+}
+
 }  // namespace bsi
 
 extern "C" {

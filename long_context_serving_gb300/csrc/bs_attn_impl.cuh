@@ -1,0 +1,773 @@
+// Device code of the sparse decode attention (a4), shared by the stand-alone kernel and
+// the fused decode step ("Technische Samenvatting: Fluxion", Probleemstelling item 1:
+// top-k selection, then sparse attention over the selected KV blocks; Kerninzichten
+// item 3: this work is bound by data movement).
+//
+// Split-KV flash-decode. A unit's selected blocks cover n_pages pages of 16 tokens;
+// they are cut into at most 32 splits of pps pages (pps a multiple of 4, chosen from
+// n_pages alone). One CTA per (split, unit):
+//   * the selection count and row are read together into shared memory; warp 0
+//     resolves page-table entries and stages pages into a two-deep ring of 4-page
+//     stages with TMA copies that complete an mbarrier with their byte count;
+//   * bf16 caches (attn_split_mma, 4 warps): each warp takes one 16-token page per
+//     stage. Pages arrive through a tiled tensor map with 128-byte swizzle, so
+//     ldmatrix reads them without bank conflicts. q.K and P.V are warp-level bf16
+//     tensor-core MMAs (m16n8k16, fp32 accumulate) with the query heads as the rows:
+//     q and K are exact in bf16; P stays in registers and enters P.V as a bf16 pair
+//     hi + lo (hi = bf16(p), lo = bf16(p - hi)), which keeps it to about 2^-16
+//     relative. Online softmax per head in fp32 with base-2 exponents; the four
+//     warps' states are combined at the end;
+//   * fp32 caches (attn_split_ffma, 8 warps): 1-D bulk copies; q.K with four threads
+//     per token over rotated 16-byte chunks, one warp per head for the softmax, and
+//     P.V with lanes owning head_dim/32 dimensions;
+//   * a unit with one split writes its output directly; otherwise each split writes
+//     an (o, m, l) record and takes an arrival ticket (one acquire-release atomic per
+//     CTA); the last split merges the records in split order by log-sum-exp.
+// Tokens past T inside a partial tail page are masked out of both products.
+//
+// In step mode (the fused decode step, launched as a programmatic dependent of the
+// selection kernel) a streaming unit's blocks are its forced blocks, computed from the
+// geometry, so its splits run without waiting; every other unit waits for the
+// selection kernel (griddepcontrol.wait) before reading its selection.
+#pragma once
+
+#include <cuda.h>
+#include <math.h>
+
+#include "bs_attn_plan.cuh"
+#include "bs_internal.cuh"
+
+namespace bsi {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kSelPreload = 512;  // selection entries staged in shared memory
+constexpr int kMmaThreads = 128;  // bf16 path: 4 warps, one page each per stage
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// ---------------------------------------------------------------------------
+// The block list of one unit as the attention sees it.
+// ---------------------------------------------------------------------------
+struct UnitBlocks {
+  bool ok;
+  int T, g, cnt;
+  bool computed;          // forced blocks from the geometry (streaming unit, step mode)
+  int n_sink, lo2;        // computed list: [0, n_sink) then [lo2, lo2 + cnt - n_sink)
+  const int32_t *sel;     // selection row (global), when not computed
+  const int32_t *sel_sm;  // its first kSelPreload entries in shared memory
+  UnitPages pg;
+
+  __device__ __forceinline__ int block(int i) const {
+    if (computed) return i < n_sink ? i : lo2 + (i - n_sink);
+    return i < kSelPreload ? sel_sm[i] : sel[i];
+  }
+};
+
+// Reads a unit's block list (waiting for the selection kernel in step mode unless
+// the unit is streaming) and its split plan. All NT threads call it.
+template <int NT, bool kStep>
+__device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
+                                       const int32_t *sel_idx, const int32_t *sel_cnt, int u, int32_t *sel_sm,
+                                       int32_t *st) {
+  __shared__ int sh_cnt;
+  const int tid = threadIdx.x, split = blockIdx.x;
+  const int b = u / dims.n_kv_heads;
+  UnitBlocks ub;
+  ub.T = kv.seq_lens[b];
+  ub.g = cfg.block_tokens[u];
+  ub.computed = false;
+  ub.sel = sel_idx + static_cast<size_t>(u) * dims.max_sel_per_unit;
+  ub.sel_sm = sel_sm;
+  ub.n_sink = ub.lo2 = 0;
+  ub.cnt = 0;
+  const bool cfg_ok = ub.g > 0 && ub.g % kPage == 0 && ub.T >= 1;
+  if (kStep) {
+    if (cfg.cls[u] == BS_STREAMING && cfg_ok) {
+      const Geom ge = unit_geom(ub.T, ub.g, cfg.sub_tokens[u], cfg.sink_tokens[u], cfg.local_tokens[u]);
+      ub.computed = true;
+      ub.n_sink = ge.n_sink;
+      ub.lo2 = ge.local_lo > ge.n_sink ? ge.local_lo : ge.n_sink;
+      ub.cnt = ge.n_sink + (ge.n_blk - ub.lo2);
+    } else {
+      pdl_wait();  // the selection kernel has finished and its writes are visible
+    }
+  }
+  if (!ub.computed) {
+    const int ns = min(dims.max_sel_per_unit, kSelPreload);
+    if (tid == 0) sh_cnt = sel_cnt[u];
+    for (int i = tid; i < ns; i += NT) sel_sm[i] = ub.sel[i];
+    __syncthreads();
+    ub.cnt = sh_cnt;
+  }
+  ub.ok = cfg_ok && ub.cnt >= 0 && ub.cnt <= dims.max_sel_per_unit;
+  if (!ub.ok && split == 0 && tid == 0) report(st, BS_ERR_INVALID_ARG);
+  int last = -1;
+  if (ub.ok && ub.cnt > 0) {
+    last = ub.block(ub.cnt - 1);
+    if (last < 0 || static_cast<int64_t>(last) * ub.g >= ub.T) {
+      if (split == 0 && tid == 0) report(st, BS_ERR_DEVICE_BOUNDS);
+      ub.ok = false;
+    }
+  }
+  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last);
+  return ub;
+}
+
+// Zero output and lse = -inf for a unit with nothing to attend (split 0 writes).
+template <int NT, int D, int G>
+__device__ void write_empty_output(float *out, float *lse, size_t orow0) {
+  constexpr int QD = D / 4;
+  if (blockIdx.x != 0) return;
+  for (int i = threadIdx.x; i < G * QD; i += NT) {
+    reinterpret_cast<float4 *>(out + (orow0 + i / QD) * D)[i % QD] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i % QD == 0) lse[orow0 + i / QD] = -INFINITY;
+  }
+}
+
+// Resolves page slot `lane` (< kStagePages) of a stage: returns the physical page and
+// the number of valid tokens in it (0 for an empty or out-of-range slot).
+__device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims &dims, const int32_t *pt, int gp,
+                                            int gp1, int *phys_out, int32_t *st) {
+  *phys_out = -1;
+  if (gp >= gp1) return 0;
+  const int ppb = ub.pg.ppb;
+  const int i = gp / ppb, pb = gp - i * ppb;
+  const int c = ub.block(i);
+  const int lp = c * ppb + pb;
+  const int t0 = lp * kPage;
+  if (c < 0 || lp >= dims.max_pages_per_unit || t0 >= ub.T) {
+    report(st, BS_ERR_DEVICE_BOUNDS);
+    return 0;
+  }
+  const int phys = __ldg(pt + lp);
+  if (phys < 0 || phys >= dims.n_pages) {
+    report(st, BS_ERR_DEVICE_BOUNDS);
+    return 0;
+  }
+  *phys_out = phys;
+  return min(kPage, ub.T - t0);
+}
+
+// Epilogue shared by both paths. `o_sm` holds this split's unnormalised output
+// [G][D] (fp32, shared), `m_sm`/`l_sm` its per-head max (log2 units) and sum. A
+// single split writes out/lse; otherwise the record is published, a ticket taken and
+// the last split merges all records in split order. `scratch` needs
+// 3 * kMaxG * kAttnMaxSplits floats of shared memory. All NT threads call it.
+template <int NT, int D, int G>
+__device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const float *o_sm, const float *m_sm,
+                             const float *l_sm, int32_t *arrivals, float *ws, float *out, float *lse, float *scratch) {
+  constexpr int QD = D / 4;
+  constexpr int REC = attn_record_floats(D);
+  __shared__ int is_last;
+  __shared__ float ML[2][kMaxG];
+  const int tid = threadIdx.x, split = blockIdx.x;
+  if (ub.pg.n_split == 1) {
+    for (int i = tid; i < G * QD; i += NT) {
+      const int h = i / QD, dq = i % QD;
+      float4 o = reinterpret_cast<const float4 *>(o_sm + h * D)[dq];
+      const float inv = 1.0f / l_sm[h];
+      o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+      reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+      if (dq == 0) lse[orow0 + h] = (m_sm[h] + log2f(l_sm[h])) * kLn2;
+    }
+    return;
+  }
+  float *rec = ws + (static_cast<size_t>(u) * kAttnMaxSplits + split) * G * REC;
+  for (int i = tid; i < G * QD; i += NT) {
+    const int h = i / QD, dq = i % QD;
+    reinterpret_cast<float4 *>(rec + h * REC)[dq] = reinterpret_cast<const float4 *>(o_sm + h * D)[dq];
+  }
+  if (tid < G) {
+    rec[tid * REC + D] = m_sm[tid];
+    rec[tid * REC + D + 1] = l_sm[tid];
+  }
+  // Publish the record and take an arrival ticket: the CTA barrier orders every
+  // thread's record writes before thread 0's release; the last split acquires.
+  __syncthreads();
+  if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == ub.pg.n_split - 1);
+  __syncthreads();
+  if (!is_last) return;
+  // Merge: M = max m_i, L = sum l_i 2^(m_i - M), o = sum 2^(m_i - M) o_i / L,
+  // lse = ln 2 (M + log2 L); splits are visited in index order.
+  const int ns = ub.pg.n_split;
+  const float *base = ws + static_cast<size_t>(u) * kAttnMaxSplits * G * REC;
+  float *m_all = scratch;                          // [G][32]
+  float *l_all = m_all + kMaxG * kAttnMaxSplits;
+  float *w_all = l_all + kMaxG * kAttnMaxSplits;
+  for (int i = tid; i < G * ns; i += NT) {
+    const int h = i / ns, sp = i % ns;
+    const float *r = base + (static_cast<size_t>(sp) * G + h) * REC;
+    m_all[h * kAttnMaxSplits + sp] = __ldcg(r + D);
+    l_all[h * kAttnMaxSplits + sp] = __ldcg(r + D + 1);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, m_all[tid * kAttnMaxSplits + sp]);
+    float Lsum = 0.0f;
+    for (int sp = 0; sp < ns; ++sp) {
+      const float mi = m_all[tid * kAttnMaxSplits + sp];
+      const float w = (mi == -INFINITY) ? 0.0f : exp2f(mi - M);
+      w_all[tid * kAttnMaxSplits + sp] = w;
+      Lsum = fmaf(l_all[tid * kAttnMaxSplits + sp], w, Lsum);
+    }
+    ML[0][tid] = M;
+    ML[1][tid] = Lsum;
+  }
+  __syncthreads();
+  constexpr int kBatch = 8;
+  for (int i = tid; i < G * QD; i += NT) {
+    const int h = i / QD, dq = i % QD;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < ns; sp0 += kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (sp0 + j < ns)
+          v[j] = __ldcg(reinterpret_cast<const float4 *>(base + (static_cast<size_t>(sp0 + j) * G + h) * REC) + dq);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (sp0 + j < ns) {
+          const float w = w_all[h * kAttnMaxSplits + sp0 + j];
+          o.x = fmaf(v[j].x, w, o.x);
+          o.y = fmaf(v[j].y, w, o.y);
+          o.z = fmaf(v[j].z, w, o.z);
+          o.w = fmaf(v[j].w, w, o.w);
+        }
+    }
+    const float inv = 1.0f / ML[1][h];
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+    if (dq == 0) lse[orow0 + h] = (ML[0][h] + log2f(ML[1][h])) * kLn2;
+  }
+  if (tid == 0) arrivals[u] = 0;  // ready for the next call
+}
+
+// ===========================================================================
+// bf16 path: tiled TMA + warp-level tensor-core MMA
+// ===========================================================================
+template <int D>
+struct MmaLayout {
+  static constexpr int kHalves = D / 64;               // 128-byte-wide column halves of a row
+  static constexpr int kHalfBytes = kPage * 128;       // 16 rows x 128 B = 2 KiB (swizzle atom x2)
+  static constexpr int kPageBytes = kHalves * kHalfBytes;
+  static constexpr int kStageKV = kStagePages * kPageBytes;  // K (or V) of one stage
+  static constexpr int kBufBytes = 2 * kStageKV;              // K then V
+  static constexpr int kOffSel = 2 * kBufBytes;
+  static constexpr int kOffQlo = kOffSel + kSelPreload * 4;    // [D/16][2][32] remainder fragments
+  static constexpr int kBytes = kOffQlo + (D / 16) * 2 * 32 * 4;
+  // After the last stage: warp states [4][8][D] and (m, l) reuse buffer 0; the merge's
+  // scratch reuses buffer 1.
+  static_assert(4 * kMaxG * D * 4 + 2 * 4 * kMaxG * 4 <= kBufBytes, "combine scratch");
+  static_assert(3 * kMaxG * kAttnMaxSplits * 4 <= kBufBytes, "merge scratch");
+};
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A B + C for m16n8k16, bf16 inputs, fp32 accumulators, keeping only rows 0..7.
+// Rows 8..15 of A are padding heads: their A registers are 0, their C inputs are 0 and
+// their D outputs go to dead temporaries, so they cost no live registers.
+__device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  float t2, t3;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %10, %10};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(t2), "=f"(t3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Byte offset of 16-byte chunk `c` (0..D/8-1) of row `r` (0..15) inside a page tile
+// written by a 128-byte-swizzled TMA box per column half.
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * (kPage * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+template <int D, int G, bool kStep>
+__device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
+                               const bs_head_cfg &cfg, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                               const int32_t *__restrict__ sel_idx, const int32_t *__restrict__ sel_cnt,
+                               int32_t *__restrict__ arrivals, float *__restrict__ ws, float *__restrict__ out,
+                               float *__restrict__ lse, int32_t *st, unsigned char *smem) {
+  using L = MmaLayout<D>;
+  constexpr int NT = kMmaThreads;
+  constexpr int KSTEPS = D / 16;
+  constexpr int NTILES = D / 8;
+  __shared__ uint64_t bars[2];
+  __shared__ int slot_valid[2][kStagePages];
+
+  const int u = blockIdx.y, split = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
+  const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
+  int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
+
+  const UnitBlocks ub = load_unit_blocks<NT, kStep>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st);
+  if (!ub.ok || ub.pg.n_pages == 0) {
+    write_empty_output<NT, D, G>(out, lse, orow0);
+    return;
+  }
+  if (split >= ub.pg.n_split) return;
+  const int gp0 = split * ub.pg.pps;
+  const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
+  const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
+  const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // Warp 0: resolve the 4 pages of a stage and start their copies (one TMA box per
+  // 64-column half of a page, for K and for V).
+  auto issue = [&](int stage, int buf) {
+    int phys = -1, valid_tok = 0;
+    if (lane < kStagePages) valid_tok = resolve_page(ub, dims, pt, gp0 + stage * kStagePages + lane, gp1, &phys, st);
+    const unsigned m = __ballot_sync(0xffffffffu, valid_tok > 0);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[buf], static_cast<uint32_t>(__popc(m)) * 2u * L::kPageBytes);
+    __syncwarp();
+    if (valid_tok > 0) {
+      fence_proxy_async_smem();
+      unsigned char *kdst = smem + buf * L::kBufBytes + lane * L::kPageBytes;
+      unsigned char *vdst = kdst + L::kStageKV;
+#pragma unroll
+      for (int hh = 0; hh < L::kHalves; ++hh) {
+        tma_load_2d(kdst + hh * L::kHalfBytes, tmk, hh * 64, phys * kPage, &bars[buf]);
+        tma_load_2d(vdst + hh * L::kHalfBytes, tmv, hh * 64, phys * kPage, &bars[buf]);
+      }
+    }
+    if (lane < kStagePages) slot_valid[buf][lane] = valid_tok;
+  };
+  if (warp == 0) {
+    issue(0, 0);
+    if (n_stages > 1) issue(1, 1);
+  }
+
+  // Query rows as MMA A fragments (rows = heads; rows >= G are zero). For an fp32
+  // query a second bf16 fragment carries the remainder q - bf16(q).
+  const bool q32 = dims.q_dtype == BS_FP32;
+  const int hrow = lane >> 2, qcol = 2 * (lane & 3);
+  uint32_t *qlo_sm = reinterpret_cast<uint32_t *>(smem + L::kOffQlo);
+  uint32_t qa_hi[KSTEPS][2];
+#pragma unroll
+  for (int kk = 0; kk < KSTEPS; ++kk)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      qa_hi[kk][j] = 0u;
+      uint32_t lo = 0u;
+      if (hrow < G) {
+        const size_t idx = (orow0 + hrow) * D + kk * 16 + j * 8 + qcol;
+        if (!q32) {
+          qa_hi[kk][j] = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(q) + idx);
+        } else {
+          const float2 qf = *reinterpret_cast<const float2 *>(static_cast<const float *>(q) + idx);
+          qa_hi[kk][j] = pack_bf16(qf.x, qf.y);
+          lo = pack_bf16(qf.x - bf16_lo_f(qa_hi[kk][j]), qf.y - bf16_hi_f(qa_hi[kk][j]));
+        }
+      }
+      if (q32 && warp == 0) qlo_sm[(kk * 2 + j) * 32 + lane] = lo;
+    }
+  if (q32) __syncthreads();
+  const float qk_scale = rsqrtf(static_cast<float>(D)) * kLog2e;
+
+  float m_run = -INFINITY, l_run = 0.0f;   // head hrow (replicated over the lane quad)
+  float o[NTILES][2];   // O[head hrow][nd*8 + qcol + {0,1}]
+#pragma unroll
+  for (int nd = 0; nd < NTILES; ++nd) o[nd][0] = o[nd][1] = 0.0f;
+
+  for (int it = 0; it < n_stages; ++it) {
+    const int buf = it & 1;
+    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st);
+    if (__syncthreads_or(!ok)) return;
+    const int valid = slot_valid[buf][warp];
+    if (valid > 0) {
+      unsigned char *kpg = smem + buf * L::kBufBytes + warp * L::kPageBytes;
+      unsigned char *vpg = kpg + L::kStageKV;
+      if (valid < kPage) {
+        // Rows past T may hold anything (even NaN): zero them in V; their scores are
+        // masked below.
+        for (int i = lane; i < (kPage - valid) * (D / 8); i += 32) {
+          const int r = valid + i / (D / 8), c = i % (D / 8);
+          *reinterpret_cast<uint4 *>(vpg + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+      }
+      // ---- S = q K^T for the 16 tokens (two n-tiles of 8) ----------------------
+      float s[2][2];   // S[head hrow][nt*8 + qcol + {0,1}]
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = 0.0f;
+      const uint32_t kbase = smem_u32(kpg);
+      const int lrow = ((lane >> 4) << 3) + (lane & 7);   // token row this lane addresses
+      const int lsub = (lane >> 3) & 1;                  // low / high 8 columns of the k-step
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz(lrow, 2 * kk + lsub), b0, b1, b2, b3);
+        mma_bf16(s[0], qa_hi[kk][0], qa_hi[kk][1], b0, b1);
+        mma_bf16(s[1], qa_hi[kk][0], qa_hi[kk][1], b2, b3);
+        if (q32) {
+          const uint32_t l0 = qlo_sm[(kk * 2) * 32 + lane], l1 = qlo_sm[(kk * 2 + 1) * 32 + lane];
+          mma_bf16(s[0], l0, l1, b0, b1);
+          mma_bf16(s[1], l0, l1, b2, b3);
+        }
+      }
+      // ---- online softmax over this page (rows = heads, quad = 16 tokens) -------
+      float x[2][2];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int t = nt * 8 + qcol + j;
+          x[nt][j] = t < valid ? s[nt][j] * qk_scale : -INFINITY;
+          mx = fmaxf(mx, x[nt][j]);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      float alpha = 1.0f, psum = 0.0f;
+      float p[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) p[nt][j] = 0.0f;
+      if (m_new != -INFINITY) {
+        alpha = exp2f(m_run - m_new);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            p[nt][j] = exp2f(x[nt][j] - m_new);
+            psum += p[nt][j];
+          }
+      }
+      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+      l_run = l_run * alpha + psum;
+      m_run = m_new;
+#pragma unroll
+      for (int nd = 0; nd < NTILES; ++nd) {
+        o[nd][0] *= alpha;
+        o[nd][1] *= alpha;
+      }
+      // P as bf16 hi + lo A fragments (k = the 16 tokens).
+      const uint32_t ph0 = pack_bf16(p[0][0], p[0][1]);
+      const uint32_t ph1 = pack_bf16(p[1][0], p[1][1]);
+      const uint32_t pl0 = pack_bf16(p[0][0] - bf16_lo_f(ph0), p[0][1] - bf16_hi_f(ph0));
+      const uint32_t pl1 = pack_bf16(p[1][0] - bf16_lo_f(ph1), p[1][1] - bf16_hi_f(ph1));
+      // ---- O += P V: V^T fragments by transposed ldmatrix -----------------------
+      const uint32_t vbase = smem_u32(vpg);
+      const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);   // token row this lane addresses
+      const int vsub = lane >> 4;                            // which of two 8-column chunks
+#pragma unroll
+      for (int nd2 = 0; nd2 < NTILES / 2; ++nd2) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vbase + swz(vrow, 2 * nd2 + vsub), v0, v1, v2, v3);
+        mma_bf16(o[2 * nd2], ph0, ph1, v0, v1);
+        mma_bf16(o[2 * nd2], pl0, pl1, v0, v1);
+        mma_bf16(o[2 * nd2 + 1], ph0, ph1, v2, v3);
+        mma_bf16(o[2 * nd2 + 1], pl0, pl1, v2, v3);
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && it + 2 < n_stages) issue(it + 2, buf);
+  }
+
+  // ---- combine the four warps' states ---------------------------------------------
+  float *ow = reinterpret_cast<float *>(smem);               // [4][8][D] in buffer 0
+  float *mw = ow + 4 * kMaxG * D;                            // [4][8]
+  float *lw = mw + 4 * kMaxG;                                // [4][8]
+  if (hrow < G) {
+#pragma unroll
+    for (int nd = 0; nd < NTILES; ++nd)
+      *reinterpret_cast<float2 *>(ow + (warp * kMaxG + hrow) * D + nd * 8 + qcol) = make_float2(o[nd][0], o[nd][1]);
+    if ((lane & 3) == 0) {
+      mw[warp * kMaxG + hrow] = m_run;
+      lw[warp * kMaxG + hrow] = l_run;
+    }
+  }
+  __syncthreads();
+  __shared__ float mfin[kMaxG], lfin[kMaxG], wfin[4][kMaxG];
+  if (tid < G) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, mw[w * kMaxG + tid]);
+    float Ls = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mi = mw[w * kMaxG + tid];
+      const float wt = (mi == -INFINITY) ? 0.0f : exp2f(mi - M);
+      wfin[w][tid] = wt;
+      Ls = fmaf(lw[w * kMaxG + tid], wt, Ls);
+    }
+    mfin[tid] = M;
+    lfin[tid] = Ls;
+  }
+  __syncthreads();
+  float *osum = reinterpret_cast<float *>(smem + L::kBufBytes);   // [G][D] in buffer 1
+  for (int i = tid; i < G * D / 4; i += NT) {
+    const int h = i / (D / 4), dq = i % (D / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float wt = wfin[w][h];
+      const float4 v = reinterpret_cast<const float4 *>(ow + (w * kMaxG + h) * D)[dq];
+      acc.x = fmaf(v.x, wt, acc.x);
+      acc.y = fmaf(v.y, wt, acc.y);
+      acc.z = fmaf(v.z, wt, acc.z);
+      acc.w = fmaf(v.w, wt, acc.w);
+    }
+    reinterpret_cast<float4 *>(osum + h * D)[dq] = acc;
+  }
+  __syncthreads();
+  finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, arrivals, ws, out, lse,
+                         reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4));
+}
+
+// ===========================================================================
+// fp32 path: 1-D bulk copies + FFMA
+// ===========================================================================
+constexpr int kFfmaThreads = 256;  // 8 warps
+
+template <int D, int G>
+struct FfmaLayout {
+  static constexpr int kPageBytes = kPage * D * 4;
+  static constexpr int kStageBytes = kStagePages * kPageBytes;
+  static constexpr int kGP = (G + 3) & ~3;  // p row stride (floats)
+  static constexpr int kOffQ = 4 * kStageBytes;
+  static constexpr int kOffS = kOffQ + G * D * 4;
+  static constexpr int kOffP = kOffS + G * kStageTokens * 4;
+  static constexpr int kOffA = kOffP + kStageTokens * kGP * 4;
+  static constexpr int kOffSel = kOffA + kMaxG * 4;
+  static constexpr int kBytes = kOffSel + kSelPreload * 4;
+  static_assert(2 * kStageBytes >= 8 * G * D * 4 + G * D * 4, "reduction scratch must fit in the K stages");
+  static_assert(2 * kStageBytes >= 3 * kMaxG * kAttnMaxSplits * 4, "merge scratch must fit in the V stages");
+};
+
+template <int D, int G, bool kStep>
+__device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
+                                const bs_head_cfg &cfg, const int32_t *__restrict__ sel_idx,
+                                const int32_t *__restrict__ sel_cnt, int32_t *__restrict__ arrivals,
+                                float *__restrict__ ws, float *__restrict__ out, float *__restrict__ lse,
+                                int32_t *st, unsigned char *smem) {
+  using L = FfmaLayout<D, G>;
+  constexpr int NT = kFfmaThreads;
+  constexpr int DPL = D / 32;
+  constexpr int kPer = D / 16;  // 16-byte chunks per quarter of a row (fp32: D/4 chunks per row)
+  __shared__ uint64_t bars[2];
+  __shared__ int slot_valid[2][kStagePages];
+  __shared__ float ml_sm[2][kMaxG];
+
+  const int u = blockIdx.y, split = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
+  const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
+  int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
+
+  const UnitBlocks ub = load_unit_blocks<NT, kStep>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st);
+  if (!ub.ok || ub.pg.n_pages == 0) {
+    write_empty_output<NT, D, G>(out, lse, orow0);
+    return;
+  }
+  if (split >= ub.pg.n_split) return;
+  const int gp0 = split * ub.pg.pps;
+  const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
+  const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
+  const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+  const unsigned char *kpool = static_cast<const unsigned char *>(kv.k_pool);
+  const unsigned char *vpool = static_cast<const unsigned char *>(kv.v_pool);
+
+  float *qs = reinterpret_cast<float *>(smem + L::kOffQ);
+  float *s_sm = reinterpret_cast<float *>(smem + L::kOffS);
+  float *p_sm = reinterpret_cast<float *>(smem + L::kOffP);
+  float *alpha_sm = reinterpret_cast<float *>(smem + L::kOffA);
+
+  if (tid == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int stage, int buf) {
+    int phys = -1, valid_tok = 0;
+    if (lane < kStagePages) valid_tok = resolve_page(ub, dims, pt, gp0 + stage * kStagePages + lane, gp1, &phys, st);
+    const unsigned m = __ballot_sync(0xffffffffu, valid_tok > 0);
+    if (lane == 0) mbar_arrive_expect_tx(&bars[buf], static_cast<uint32_t>(__popc(m)) * 2u * L::kPageBytes);
+    __syncwarp();
+    if (valid_tok > 0) {
+      fence_proxy_async_smem();
+      const size_t src = static_cast<size_t>(phys) * L::kPageBytes;
+      bulk_g2s(smem + buf * L::kStageBytes + lane * L::kPageBytes, kpool + src, L::kPageBytes, &bars[buf]);
+      bulk_g2s(smem + (2 + buf) * L::kStageBytes + lane * L::kPageBytes, vpool + src, L::kPageBytes, &bars[buf]);
+    }
+    if (lane < kStagePages) slot_valid[buf][lane] = valid_tok;
+  };
+
+  if (warp == 0) {
+    issue(0, 0);
+    if (n_stages > 1) issue(1, 1);
+  }
+  {
+    const float qscale = rsqrtf(static_cast<float>(D)) * kLog2e;
+    const size_t qbase = orow0 * D;
+    for (int i = tid; i < G * D; i += NT) qs[i] = load_scalar(q, qbase + i, dims.q_dtype) * qscale;
+  }
+
+  float m_run = -INFINITY, l_run = 0.0f;
+  float acc[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[h][j] = 0.0f;
+
+  const int tok = tid >> 2, qq = tid & 3;
+  for (int it = 0; it < n_stages; ++it) {
+    const int buf = it & 1;
+    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st);
+    if (__syncthreads_or(!ok)) return;
+
+    const unsigned char *Kb = smem + buf * L::kStageBytes;
+    const bool tvalid = (tok & (kPage - 1)) < slot_valid[buf][tok >> 4];
+    float a[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) a[h] = 0.0f;
+    if (tvalid) {
+      const float4 *row = reinterpret_cast<const float4 *>(Kb + tok * D * 4);
+#pragma unroll
+      for (int c = 0; c < kPer; ++c) {
+        const int ch = qq + 4 * ((c + tok) & (kPer - 1));
+        const float4 k4 = row[ch];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 q4 = reinterpret_cast<const float4 *>(qs + h * D)[ch];
+          a[h] = fmaf(q4.x, k4.x, a[h]);
+          a[h] = fmaf(q4.y, k4.y, a[h]);
+          a[h] = fmaf(q4.z, k4.z, a[h]);
+          a[h] = fmaf(q4.w, k4.w, a[h]);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      a[h] += __shfl_xor_sync(0xffffffffu, a[h], 1);
+      a[h] += __shfl_xor_sync(0xffffffffu, a[h], 2);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      if ((h & 3) == qq) s_sm[h * kStageTokens + tok] = tvalid ? a[h] : -INFINITY;
+    __syncthreads();
+
+    if (warp < G) {
+      const float s0 = s_sm[warp * kStageTokens + lane];
+      const float s1 = s_sm[warp * kStageTokens + lane + 32];
+      float mx = fmaxf(s0, s1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float m_new = fmaxf(m_run, mx);
+      float alpha = 1.0f, p0 = 0.0f, p1 = 0.0f;
+      if (m_new != -INFINITY) {
+        alpha = exp2f(m_run - m_new);
+        p0 = exp2f(s0 - m_new);
+        p1 = exp2f(s1 - m_new);
+      }
+      float ps = p0 + p1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l_run = l_run * alpha + ps;
+      m_run = m_new;
+      p_sm[lane * L::kGP + warp] = p0;
+      p_sm[(lane + 32) * L::kGP + warp] = p1;
+      if (lane == 0) alpha_sm[warp] = alpha;
+    }
+    __syncthreads();
+
+    {
+      float al[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) al[h] = alpha_sm[h];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc[h][j] *= al[h];
+      const float *Vb = reinterpret_cast<const float *>(smem + (2 + buf) * L::kStageBytes);
+#pragma unroll 2
+      for (int i = 0; i < kStageTokens / 8; ++i) {
+        const int t = warp + 8 * i;
+        if ((t & (kPage - 1)) >= slot_valid[buf][t >> 4]) continue;  // warp-uniform
+        float v[DPL];
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) v[j] = Vb[t * D + lane * DPL + j];
+        float p[L::kGP];
+#pragma unroll
+        for (int h4 = 0; h4 < L::kGP / 4; ++h4) {
+          const float4 pv = reinterpret_cast<const float4 *>(p_sm + t * L::kGP)[h4];
+          p[4 * h4 + 0] = pv.x; p[4 * h4 + 1] = pv.y; p[4 * h4 + 2] = pv.z; p[4 * h4 + 3] = pv.w;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int j = 0; j < DPL; ++j) acc[h][j] = fmaf(p[h], v[j], acc[h][j]);
+      }
+    }
+    __syncthreads();
+    if (warp == 0 && it + 2 < n_stages) issue(it + 2, buf);
+  }
+
+  // ---- sum the 8 warps' accumulators --------------------------------------------
+  float *red = reinterpret_cast<float *>(smem);        // [8][G][D] over the K stages
+  float *osum = red + 8 * G * D;                       // [G][D]
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) red[(warp * G + h) * D + lane * DPL + j] = acc[h][j];
+  if (warp < G && lane == 0) {
+    ml_sm[0][warp] = m_run;
+    ml_sm[1][warp] = l_run;
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += NT) {
+    const int h = i / D, dd = i - h * D;
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += red[(w * G + h) * D + dd];
+    osum[h * D + dd] = sum;
+  }
+  __syncthreads();
+  finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], arrivals, ws, out, lse,
+                         reinterpret_cast<float *>(smem + 2 * L::kStageBytes));
+}
+
+}  // namespace bsi

@@ -14,8 +14,16 @@ constexpr int kAttnMaxSplits = 32;                 // splits per unit, at most
 // One partial record per (unit, split, head): o[D] (unnormalised), m (log2 units), l, 2 pad.
 __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 
-// The workspace starts with one int32 arrival counter per unit, padded to 16 bytes.
-__host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (units + 3) / 4 * 4; }
+// The workspace starts with two int32 arrival counters per unit (the selection phase
+// of the fused decode step, then the attention), padded to 16 bytes.
+__host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (2 * units + 3) / 4 * 4; }
+
+// Splits launched per unit: enough for the largest gathered page count.
+__host__ __device__ inline int attn_grid_splits(int max_gather_pages) {
+  int splits = (max_gather_pages + kStagePages - 1) / kStagePages;
+  if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
+  return splits < 1 ? 1 : splits;
+}
 
 // Pages covered by a unit's selection: every selected block but the last is complete
 // (only the tail block can be partial and it has the largest index).

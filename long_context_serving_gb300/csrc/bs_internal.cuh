@@ -1,6 +1,7 @@
 // Internal helpers shared by the kernels of libbsattn (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -61,6 +62,11 @@ __host__ __device__ __forceinline__ bool unit_cfg_ok(int cls, int g, int s, int 
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned char *align_smem_1024(unsigned char *p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -153,6 +159,14 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Shape checks common to every call. Returns BS_OK or the first problem.
 bs_status check_dims(const bs_dims *d);
+
+// Tiled tensor maps over the bf16 K and V pools viewed as [n_pages * 16][head_dim]:
+// boxes of 16 rows x 64 columns (128 bytes) with 128-byte swizzle.
+bs_status make_kv_tensor_maps(const bs_dims &d, const bs_kv &kv, CUtensorMap *tk, CUtensorMap *tv);
+
+// Dynamic shared memory is re-based to a 1024-byte boundary (the 128-byte swizzle
+// atom of TMA copies); kernels that need it allocate this much more.
+constexpr int kSmemAlignSlack = 1024;
 
 inline bs_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? BS_OK : BS_ERR_CUDA;

@@ -1,55 +1,14 @@
-// a5: set-difference of the selection against the previous step ("Technisches
-// Resümee: NOSA", Methodik / 2. System: NOSI: set-difference kernels for block
-// swapping).
-//
-// One CTA per unit. Both ascending lists are staged in shared memory; each element
-// of one list is looked up in the other by binary search, and the misses are
-// compacted in order, so both outputs come out ascending.
-#include "bs_internal.cuh"
+// a5: set-difference of the selection against the previous step, stand-alone kernel
+// ("Technisches Resümee: NOSA", Methodik / 2. System: NOSI: set-difference kernels
+// for block swapping). One CTA per unit; both ascending lists are staged in shared
+// memory; each element of one list is looked up in the other by binary search and the
+// misses are compacted in order, so both outputs come out ascending.
+#include "bs_select_impl.cuh"
 
 namespace bsi {
 namespace {
 
 constexpr int kDiffThreads = 256;
-constexpr int kDiffWarps = kDiffThreads / 32;
-
-__device__ __forceinline__ bool contains(const int32_t *v, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (v[mid] < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo < n && v[lo] == x;
-}
-
-// Writes the elements of a[0..na) missing from b[0..nb) to dst (ascending), pads
-// with -1 up to cap and returns the count.
-__device__ int diff_into(const int32_t *a, int na, const int32_t *b, int nb, int32_t *dst, int cap,
-                         int *warp_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (na + kDiffThreads - 1) / kDiffThreads;
-  const int s = tid * per, e = min(na, s + per);
-  int mine = 0;
-  for (int i = s; i < e; ++i) mine += contains(b, nb, a[i]) ? 0 : 1;
-  int x = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_tot[warp] = x;
-  __syncthreads();
-  int before = x - mine;
-  for (int w = 0; w < warp; ++w) before += warp_tot[w];
-  int total = 0;
-  for (int w = 0; w < kDiffWarps; ++w) total += warp_tot[w];
-  for (int i = s; i < e; ++i)
-    if (!contains(b, nb, a[i])) dst[before++] = a[i];
-  for (int i = total + tid; i < cap; i += kDiffThreads) dst[i] = -1;
-  __syncthreads();
-  return total;
-}
 
 __global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(bs_dims dims, const int32_t *__restrict__ prev,
                                                                const int32_t *__restrict__ prev_cnt,
@@ -60,7 +19,7 @@ __global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(bs_dims dims, con
                                                                int32_t *__restrict__ removed,
                                                                int32_t *__restrict__ removed_cnt, int32_t *st) {
   extern __shared__ __align__(16) int32_t lists[];
-  __shared__ int warp_tot[kDiffWarps];
+  __shared__ SelShared<kDiffThreads> sh;
   const int cap = dims.max_sel_per_unit;
   const int u = blockIdx.x, tid = threadIdx.x;
   int32_t *sp = lists, *sc = lists + cap;
@@ -78,8 +37,8 @@ __global__ void __launch_bounds__(kDiffThreads) setdiff_kernel(bs_dims dims, con
   for (int i = tid; i < np; i += kDiffThreads) sp[i] = prev[row + i];
   for (int i = tid; i < nc; i += kDiffThreads) sc[i] = cur[row + i];
   __syncthreads();
-  const int na = diff_into(sc, nc, sp, np, added + row, cap, warp_tot);
-  const int nr = diff_into(sp, np, sc, nc, removed + row, cap, warp_tot);
+  const int na = sorted_diff_into<kDiffThreads>(sc, nc, sp, np, added + row, cap, sh);
+  const int nr = sorted_diff_into<kDiffThreads>(sp, np, sc, nc, removed + row, cap, sh);
   if (tid == 0) {
     added_cnt[u] = na;
     removed_cnt[u] = nr;

@@ -170,6 +170,25 @@ class PagedLayer:
         B.block_setdiff(self.dims, self.sel[prev], self.cnt[prev], self.sel[self.cur], self.cnt[self.cur],
                         self.added, self.added_cnt, self.removed, self.removed_cnt, self.status, stream)
 
+    def step_io(self, step: int) -> B.StepIO:
+        """Buffers of bs_decode_step for ``step`` (current selection buffer ``self.cur``)."""
+        prev = 1 - self.cur
+        ptr = lambda t: 0 if t is None else t.data_ptr()  # noqa: E731
+        return B.StepIO(q=self.q[step].data_ptr(), summaries=self.summaries.data_ptr(),
+                        scores=self.scores.data_ptr(), evict_logits=ptr(self.evict), alive=ptr(self.alive),
+                        prev_idx=self.sel[prev].data_ptr(), prev_cnt=self.cnt[prev].data_ptr(),
+                        cur_idx=self.sel[self.cur].data_ptr(), cur_cnt=self.cnt[self.cur].data_ptr(),
+                        added=self.added.data_ptr(), added_cnt=self.added_cnt.data_ptr(),
+                        removed=self.removed.data_ptr(), removed_cnt=self.removed_cnt.data_ptr(),
+                        out=self.out.data_ptr(), lse=self.lse.data_ptr(), workspace=self.workspace.data_ptr(),
+                        workspace_bytes=self.workspace.numel() * 4, dev_status=self.status.data_ptr())
+
+    def fused_step(self, step: int, group_reduce=B.BS_GROUP_MAX, stream=None) -> None:
+        """The same decode step through bs_decode_step (two launches), then advance."""
+        B.decode_step(self.dims, self.kv_at(self.seq_lens[step]), self.cfg, self.step_io(step), group_reduce,
+                      stream)
+        self.advance()
+
     def advance(self) -> None:
         """The current selection becomes the previous one."""
         self.cur = 1 - self.cur

@@ -57,8 +57,15 @@ def attention_errors(o_gpu: np.ndarray, o_ref: np.ndarray):
     return float(diff.max()), float((diff / np.maximum(np.abs(o_ref), REL_FLOOR)).max())
 
 
-def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_sample=None, seed=0) -> Report:
-    """Drive the GPU path and the oracle through the same steps on ``units`` (default all)."""
+def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_sample=None, seed=0,
+               fused=False) -> Report:
+    """Drive the GPU path and the oracle through the same steps on ``units`` (default all).
+
+    ``fused``: run each step through bs_decode_step (one call for all five steps). A
+    near-tie unit whose GPU selection differs from the oracle's then cannot be given
+    the oracle's selection before attention: its attention and set-difference are not
+    compared at that step, and the oracle's selection is written back as the previous
+    selection of the next step, so both sides continue from the same state."""
     units = list(range(wl.U)) if units is None else list(units)
     reduce_code = B.BS_GROUP_MAX if group_reduce == "max" else B.BS_GROUP_MEAN
     rng = np.random.default_rng(seed)
@@ -69,12 +76,17 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
     G = wl.G
     for step in range(wl.steps if steps is None else steps):
         layer.append(step)
-        layer.update_summaries(step)
-        layer.score(step, reduce_code)
-        layer.select(step)
+        if fused:
+            layer.fused_step(step, reduce_code)         # advances: results sit in 1 - cur
+            sel_buf = 1 - layer.cur
+        else:
+            layer.update_summaries(step)
+            layer.score(step, reduce_code)
+            layer.select(step)
+            sel_buf = layer.cur
         torch.cuda.synchronize()
         res = O.decode_step(wl, step, state, units, group_reduce)
-        gsel = layer.selection(layer.cur)
+        gsel = layer.selection(sel_buf)
         scores = layer.scores.cpu().numpy()
         alive = layer.alive.cpu().numpy() if layer.alive is not None else None
         override = {}
@@ -88,14 +100,15 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
             gs = layer.unit_summaries(u, n_sub)
             rep.sum_abs = max(rep.sum_abs, float(np.abs(gs[rows] - state[u].kbar[rows]).max()))
             if wl.cls[u] != O.STREAMING:
-                # a2: scores on candidates, -inf elsewhere
+                # a2: scores on candidates (-inf elsewhere from the stand-alone call)
                 C = O.candidate_blocks(r.T, g, int(wl.sink[u]), int(wl.local[u]))
                 if C:
                     err = np.abs(scores[u, C] - r.scores[C]) - SCORE_REL * np.abs(r.scores[C])
                     rep.score_abs = max(rep.score_abs, float(err.max()))
-                mask = np.ones(layer.max_blocks, bool)
-                mask[C] = False
-                assert np.all(scores[u, mask] == -np.inf), (step, u)
+                if not fused:
+                    mask = np.ones(layer.max_blocks, bool)
+                    mask[C] = False
+                    assert np.all(scores[u, mask] == -np.inf), (step, u)
             # a3: selection
             if r.sel.near_tie:
                 rep.near_ties += 1
@@ -107,10 +120,16 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
             if wl.cls[u] == O.DUAL:
                 n_blk = -(-r.T // g)
                 assert np.array_equal(alive[u, :n_blk], r.sel.alive[:n_blk]), (step, u)
-        if override:
-            layer.set_selection(override)
-        layer.attend(step)
-        layer.setdiff()
+        if fused:
+            skip = set(override)
+            if override:
+                layer.set_selection(override, which=sel_buf)
+        else:
+            skip = set()
+            if override:
+                layer.set_selection(override)
+            layer.attend(step)
+            layer.setdiff()
         torch.cuda.synchronize()
         out = layer.out.cpu().numpy()
         lse = layer.lse.cpu().numpy()
@@ -120,6 +139,8 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
         removed_cnt = layer.removed_cnt.cpu().numpy()
         for u in units:
             r = res[u]
+            if u in skip:
+                continue
             b, hk = divmod(u, wl.Hkv)
             a_abs, a_rel = attention_errors(out[b, hk * G:(hk + 1) * G], r.o)
             rep.att_abs, rep.att_rel = max(rep.att_abs, a_abs), max(rep.att_rel, a_rel)
@@ -128,7 +149,8 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
             assert removed[u, :removed_cnt[u]].tolist() == r.removed, (step, u)
             assert (added[u, added_cnt[u]:] == -1).all() and (removed[u, removed_cnt[u]:] == -1).all()
             rep.compared_units += 1
-        layer.advance()
+        if not fused:
+            layer.advance()
         status = layer.read_status()
         assert status == 0, f"device status {status}: {B.status_string(status)}"
     return rep

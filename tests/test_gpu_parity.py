@@ -39,6 +39,45 @@ def test_parity_small(name):
     rep.check()
 
 
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_parity_small_fused_step(name):
+    cfg, kw = SMALL[name]
+    rep = run_parity(make_workload(cfg, seed=1, **kw), fused=True)
+    rep.check()
+
+
+@pytest.mark.parametrize("cfg,n_units", [(2, None), (3, 6), (4, 6), (5, 6)])
+def test_parity_full_size_fused_step(cfg, n_units):
+    wl = make_workload(cfg, seed=0)
+    units = None if n_units is None else _sample_units(wl, n_units)
+    rep = run_parity(wl, units, summary_rows_sample=None if cfg <= 2 else 256, fused=True)
+    rep.check()
+
+
+def test_fused_step_matches_separate_calls():
+    """bs_decode_step gives the separate calls' selections, set-differences and
+    summaries exactly and their attention within rounding."""
+    wl = make_workload(3, seed=13, B=2, T=7000, steps=6)
+    a, b = PagedLayer(wl), PagedLayer(wl)
+    a.prefill()
+    b.prefill()
+    for step in range(wl.steps):
+        a.append(step)
+        b.append(step)
+        a.step(step)
+        b.fused_step(step)
+        torch.cuda.synchronize()
+        assert a.selection(1 - a.cur) == b.selection(1 - b.cur), step
+        for name in ("added", "removed", "added_cnt", "removed_cnt"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), (step, name)
+        assert torch.equal(a.summaries.nan_to_num(7.0), b.summaries.nan_to_num(7.0)), step
+        assert (a.out - b.out).abs().max().item() <= 1e-5
+        assert (a.lse - b.lse).abs().max().item() <= 1e-5
+    if a.alive is not None:
+        assert torch.equal(a.alive, b.alive)
+    assert a.read_status() == 0 and b.read_status() == 0
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
