@@ -185,11 +185,13 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * and Kerninzichten item 3 (bound by data movement). For each query head h of unit
  * u, over the tokens U of the selected blocks (each clipped to t < T):
  *   out_h = sum_t softmax_t(q_h . K[t] / sqrt(d)) V[t],  lse_h = log sum_t exp(q_h . K[t] / sqrt(d)).
- * Split-KV: a unit's gathered pages are cut into at most 32 contiguous splits whose
- * size depends only on that unit's page count; each split keeps an fp32 online
- * softmax and the partials are merged by log-sum-exp.
- * The last split of a unit to finish (an int32 arrival counter per unit) merges the
- * unit's partials in split order, so the result does not depend on timing.
+ * Split-KV: a unit's gathered pages are cut into contiguous splits whose size depends
+ * only on that unit's page count; each split keeps an fp32 online softmax and the
+ * partials are merged by log-sum-exp in split order, so the result does not depend on
+ * timing. When max_gather_pages_per_unit <= 1024 a unit's 16 splits form one
+ * thread-block cluster and merge through distributed shared memory; larger
+ * selections use up to 32 splits whose partials go through the workspace, merged by
+ * the last split to finish (an int32 arrival counter per unit).
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
  * aligned. It starts with two int32 arrival counters per unit (padded to 16 bytes);
  * these must be zero before the first call: zero the workspace once after
@@ -206,11 +208,13 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * inside a host engine that owns every allocation and offers no allocator, or a
  * serving loop that may not call cudaMalloc once it runs (the call synchronises the
  * device and can fail under memory pressure). Same inputs, outputs and results as
- * bs_sparse_decode_attn, but the split partials and arrival counters live in a fixed
- * 8 MiB array inside this library's device memory, which every GPU that loads the
- * library keeps until the process exits.
- * Limit: bs_workspace_size(dims) must not exceed 8 MiB (for head_dim 128 and G = 4
- * that is 62 units); larger dims return BS_ERR_CAPACITY before anything is enqueued.
+ * bs_sparse_decode_attn, but the workspace it would take (arrival counters and, for
+ * selections above 1024 pages per unit, split partials) lives in a fixed 8 MiB array
+ * inside this library's device memory, which every GPU that loads the library keeps
+ * until the process exits.
+ * Limit: bs_workspace_size(dims) must not exceed 8 MiB (with selections above 1024
+ * pages, head_dim 128 and G = 4 that is 62 units; below, the counters alone allow a
+ * million units); larger dims return BS_ERR_CAPACITY before anything is enqueued.
  * The first call on each device looks up the array's device address with that device
  * current and caches it; make that first call before any stream capture.
  * Every call clears the arrival counters on `stream` before its kernel. All calls
@@ -256,10 +260,13 @@ typedef struct {
  * appended since the last step). Only the order of fp32 additions inside the
  * attention may differ from the separate calls (streaming units split their pages
  * differently), which stays within rounding.
- * Launch 1 scores every candidate tile; the last tile of each unit selects, writes
- * the selection and set-difference and updates a1 (that sub-block lies in the forced
- * tail block, which no score of this step reads). Launch 2 is the attention, launched
- * as a programmatic dependent: streaming units' splits start before launch 1 ends.
+ * Launch 1 scores every candidate tile; tile 0 of each unit also updates a1 (that
+ * sub-block lies in the forced tail block, which no score of this step reads); the
+ * last tile of each unit selects, publishes the selection (cur_cnt is set to -1 first
+ * and receives the count with a release store once the row is written) and writes
+ * the set-difference. Launch 2 is the attention, launched as a programmatic
+ * dependent: streaming units' splits start before launch 1 ends; the others wait,
+ * bounded, for their unit's published count.
  * Both launches may begin before the work ahead of them in `stream` has finished;
  * before waiting for it they read only the per-unit head configuration (cfg arrays),
  * so those must not be written by the kernel immediately before this call. Everything

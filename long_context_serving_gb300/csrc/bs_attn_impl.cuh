@@ -6,9 +6,10 @@
 // Split-KV flash-decode. A unit's selected blocks cover n_pages pages of 16 tokens;
 // they are cut into at most 32 splits of pps pages (pps a multiple of 4, chosen from
 // n_pages alone). One CTA per (split, unit):
-//   * the selection count and row are read together into shared memory; warp 0
-//     resolves page-table entries and stages pages into a two-deep ring of 4-page
-//     stages with TMA copies that complete an mbarrier with their byte count;
+//   * the selection count and row are read into shared memory; warp 0 resolves
+//     page-table entries and stages pages into a ring of 4-page stages (three deep for
+//     bf16, two for fp32) with TMA copies that complete an mbarrier with their byte
+//     count;
 //   * bf16 caches (attn_split_mma, 4 warps): each warp takes one 16-token page per
 //     stage. Pages arrive through a tiled tensor map with 128-byte swizzle, so
 //     ldmatrix reads them without bank conflicts. q.K and P.V are warp-level bf16
@@ -20,15 +21,21 @@
 //   * fp32 caches (attn_split_ffma, 8 warps): 1-D bulk copies; q.K with four threads
 //     per token over rotated 16-byte chunks, one warp per head for the softmax, and
 //     P.V with lanes owning head_dim/32 dimensions;
-//   * a unit with one split writes its output directly; otherwise each split writes
-//     an (o, m, l) record and takes an arrival ticket (one acquire-release atomic per
-//     CTA); the last split merges the records in split order by log-sum-exp.
+//   * merge, cluster mode (selections up to 1024 pages): a unit's 16 splits are one
+//     thread-block cluster; each keeps its (o, m, l) in shared memory and, after a
+//     cluster barrier, each CTA merges a slice of the output by log-sum-exp reading
+//     its peers' shared memory (no global traffic, no atomics);
+//   * merge, workspace mode (larger selections, up to 32 splits): a unit with one
+//     split writes its output directly; otherwise each split writes an (o, m, l)
+//     record and takes an arrival ticket (one acquire-release atomic per CTA); the
+//     last split merges the records in split order.
 // Tokens past T inside a partial tail page are masked out of both products.
 //
 // In step mode (the fused decode step, launched as a programmatic dependent of the
 // selection kernel) a streaming unit's blocks are its forced blocks, computed from the
-// geometry, so its splits run without waiting; every other unit waits for the
-// selection kernel (griddepcontrol.wait) before reading its selection.
+// geometry, so its splits run without waiting; every other unit waits (bounded) until
+// the selection kernel has published that unit's selection count with a release
+// store, then reads the row.
 #pragma once
 
 #include <cuda.h>
@@ -46,6 +53,12 @@ constexpr int kMmaThreads = 128;  // bf16 path: 4 warps, one page each per stage
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ int load_acquire_gpu(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *p, int v) {
   int old;
@@ -73,10 +86,10 @@ struct UnitBlocks {
 
 // Reads a unit's block list (waiting for the selection kernel in step mode unless
 // the unit is streaming) and its split plan. All NT threads call it.
-template <int NT, bool kStep>
+template <int NT>
 __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
                                        const int32_t *sel_idx, const int32_t *sel_cnt, int u, int32_t *sel_sm,
-                                       int32_t *st) {
+                                       int32_t *st, bool in_step, bool in_cluster) {
   __shared__ int sh_cnt;
   const int tid = threadIdx.x, split = blockIdx.x;
   const int b = u / dims.n_kv_heads;
@@ -89,23 +102,40 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
   ub.n_sink = ub.lo2 = 0;
   ub.cnt = 0;
   const bool cfg_ok = ub.g > 0 && ub.g % kPage == 0 && ub.T >= 1;
-  if (kStep) {
-    if (cfg.cls[u] == BS_STREAMING && cfg_ok) {
-      const Geom ge = unit_geom(ub.T, ub.g, cfg.sub_tokens[u], cfg.sink_tokens[u], cfg.local_tokens[u]);
-      ub.computed = true;
-      ub.n_sink = ge.n_sink;
-      ub.lo2 = ge.local_lo > ge.n_sink ? ge.local_lo : ge.n_sink;
-      ub.cnt = ge.n_sink + (ge.n_blk - ub.lo2);
-    } else {
-      pdl_wait();  // the selection kernel has finished and its writes are visible
-    }
+  if (in_step && cfg.cls[u] == BS_STREAMING && cfg_ok) {
+    const Geom ge = unit_geom(ub.T, ub.g, cfg.sub_tokens[u], cfg.sink_tokens[u], cfg.local_tokens[u]);
+    ub.computed = true;
+    ub.n_sink = ge.n_sink;
+    ub.lo2 = ge.local_lo > ge.n_sink ? ge.local_lo : ge.n_sink;
+    ub.cnt = ge.n_sink + (ge.n_blk - ub.lo2);
   }
   if (!ub.computed) {
-    const int ns = min(dims.max_sel_per_unit, kSelPreload);
-    if (tid == 0) sh_cnt = sel_cnt[u];
-    for (int i = tid; i < ns; i += NT) sel_sm[i] = ub.sel[i];
+    if (tid == 0) {
+      int c = 0;
+      if (in_step) {
+        // The selection kernel publishes this unit's count with a release store once
+        // the row is written (-1 until then). Bounded wait: about one second.
+        c = load_acquire_gpu(sel_cnt + u);
+        if (c < 0) {
+          const uint64_t t0 = global_ns();
+          while ((c = load_acquire_gpu(sel_cnt + u)) < 0) {
+            if (global_ns() - t0 > 1000000000ull) {
+              report(st, BS_ERR_TIMEOUT);
+              c = 0;
+              break;
+            }
+          }
+        }
+      } else {
+        c = sel_cnt[u];
+      }
+      sh_cnt = c;
+    }
     __syncthreads();
     ub.cnt = sh_cnt;
+    const int ns = min(min(dims.max_sel_per_unit, kSelPreload), max(ub.cnt, 0));
+    for (int i = tid; i < ns; i += NT) sel_sm[i] = in_step ? __ldcg(ub.sel + i) : ub.sel[i];
+    __syncthreads();
   }
   ub.ok = cfg_ok && ub.cnt >= 0 && ub.cnt <= dims.max_sel_per_unit;
   if (!ub.ok && split == 0 && tid == 0) report(st, BS_ERR_INVALID_ARG);
@@ -117,7 +147,7 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
       ub.ok = false;
     }
   }
-  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last);
+  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster);
   return ub;
 }
 
@@ -251,17 +281,89 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
   if (tid == 0) arrivals[u] = 0;  // ready for the next call
 }
 
+// ---------------------------------------------------------------------------
+// Cluster-mode merge through distributed shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// Every CTA of the cluster holds its split's unnormalised o [G][D], m [G] (log2
+// units) and l [G] in shared memory (an idle split: m = -inf, l = 0, o = 0). After a
+// cluster barrier CTA r merges float4 columns r, r + 16, ... of the output over the 16
+// splits in split order; a second barrier keeps every CTA alive until its peers have
+// read it. All threads of all CTAs of the cluster call it.
+template <int NT, int D, int G>
+__device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm, const float *l_sm, float *out,
+                              float *lse) {
+  constexpr int C = kClusterSplits, QD = D / 4, NF4 = G * QD;
+  cluster_sync_all();
+  const uint32_t rank = cluster_rank();
+  for (int i = static_cast<int>(rank) + C * static_cast<int>(threadIdx.x); i < NF4; i += C * NT) {
+    const int h = i / QD, dq = i % QD;
+    float mp[C], lp[C];
+    float M = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < C; ++p) {
+      mp[p] = ld_peer(peer_addr(m_sm + h, p));
+      lp[p] = ld_peer(peer_addr(l_sm + h, p));
+      M = fmaxf(M, mp[p]);
+    }
+    float Lsum = 0.0f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < C; ++p) {
+      const float w = (mp[p] == -INFINITY) ? 0.0f : exp2f(mp[p] - M);
+      Lsum = fmaf(lp[p], w, Lsum);
+      const float4 v = ld_peer4(peer_addr(o_sm + h * D + dq * 4, p));
+      o.x = fmaf(v.x, w, o.x);
+      o.y = fmaf(v.y, w, o.y);
+      o.z = fmaf(v.z, w, o.z);
+      o.w = fmaf(v.w, w, o.w);
+    }
+    const float inv = 1.0f / Lsum;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+    if (dq == 0) lse[orow0 + h] = (M + log2f(Lsum)) * kLn2;
+  }
+  cluster_sync_all();
+}
+
 // ===========================================================================
 // bf16 path: tiled TMA + warp-level tensor-core MMA
 // ===========================================================================
 template <int D>
 struct MmaLayout {
+  static constexpr int kRing = 3;                      // stages in flight
   static constexpr int kHalves = D / 64;               // 128-byte-wide column halves of a row
   static constexpr int kHalfBytes = kPage * 128;       // 16 rows x 128 B = 2 KiB (swizzle atom x2)
   static constexpr int kPageBytes = kHalves * kHalfBytes;
   static constexpr int kStageKV = kStagePages * kPageBytes;  // K (or V) of one stage
   static constexpr int kBufBytes = 2 * kStageKV;              // K then V
-  static constexpr int kOffSel = 2 * kBufBytes;
+  static constexpr int kOffSel = kRing * kBufBytes;
   static constexpr int kOffQlo = kOffSel + kSelPreload * 4;    // [D/16][2][32] remainder fragments
   static constexpr int kBytes = kOffQlo + (D / 16) * 2 * 32 * 4;
   // After the last stage: warp states [4][8][D] and (m, l) reuse buffer 0; the merge's
@@ -291,6 +393,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 // D = A B + C for m16n8k16, bf16 inputs, fp32 accumulators, keeping only rows 0..7.
 // Rows 8..15 of A are padding heads: their A registers are 0, their C inputs are 0 and
 // their D outputs go to dead temporaries, so they cost no live registers.
+#pragma nv_diag_suppress 550  // t2, t3 below are written by the MMA and deliberately unused
 __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
   float t2, t3;
   asm volatile(
@@ -299,6 +402,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2
       : "+f"(d[0]), "+f"(d[1]), "=f"(t2), "=f"(t3)
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
 }
+#pragma nv_diag_default 550
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -313,18 +417,20 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (kPage * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-template <int D, int G, bool kStep>
+template <int D, int G>
 __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
                                const bs_head_cfg &cfg, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                const int32_t *__restrict__ sel_idx, const int32_t *__restrict__ sel_cnt,
                                int32_t *__restrict__ arrivals, float *__restrict__ ws, float *__restrict__ out,
-                               float *__restrict__ lse, int32_t *st, unsigned char *smem) {
+                               float *__restrict__ lse, int32_t *st, unsigned char *smem, bool in_step,
+                               bool in_cluster) {
   using L = MmaLayout<D>;
   constexpr int NT = kMmaThreads;
   constexpr int KSTEPS = D / 16;
   constexpr int NTILES = D / 8;
-  __shared__ uint64_t bars[2];
-  __shared__ int slot_valid[2][kStagePages];
+  constexpr int R = L::kRing;
+  __shared__ uint64_t bars[R];
+  __shared__ int slot_valid[R][kStagePages];
 
   const int u = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -332,20 +438,21 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  const UnitBlocks ub = load_unit_blocks<NT, kStep>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st);
+  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);
     return;
   }
-  if (split >= ub.pg.n_split) return;
-  const int gp0 = split * ub.pg.pps;
+  // In cluster mode a split without pages stays to take part in the merge.
+  if (!in_cluster && split >= ub.pg.n_split) return;
+  const int gp0 = min(split * ub.pg.pps, ub.pg.n_pages);
   const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
   const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
   const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
 
   if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+#pragma unroll
+    for (int i = 0; i < R; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -370,10 +477,8 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
     }
     if (lane < kStagePages) slot_valid[buf][lane] = valid_tok;
   };
-  if (warp == 0) {
-    issue(0, 0);
-    if (n_stages > 1) issue(1, 1);
-  }
+  if (warp == 0)
+    for (int i = 0; i < R && i < n_stages; ++i) issue(i, i);
 
   // Query rows as MMA A fragments (rows = heads; rows >= G are zero). For an fp32
   // query a second bf16 fragment carries the remainder q - bf16(q).
@@ -408,9 +513,11 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   for (int nd = 0; nd < NTILES; ++nd) o[nd][0] = o[nd][1] = 0.0f;
 
   for (int it = 0; it < n_stages; ++it) {
-    const int buf = it & 1;
-    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st);
-    if (__syncthreads_or(!ok)) return;
+    const int buf = it % R;
+    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it / R) & 1), st);
+    // A copy that never lands: stop computing but still reach the merge (the status
+    // word holds BS_ERR_TIMEOUT and the output is not meaningful).
+    if (__syncthreads_or(!ok)) break;
     const int valid = slot_valid[buf][warp];
     if (valid > 0) {
       unsigned char *kpg = smem + buf * L::kBufBytes + warp * L::kPageBytes;
@@ -502,7 +609,7 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
       }
     }
     __syncthreads();
-    if (warp == 0 && it + 2 < n_stages) issue(it + 2, buf);
+    if (warp == 0 && it + R < n_stages) issue(it + R, buf);
   }
 
   // ---- combine the four warps' states ---------------------------------------------
@@ -552,8 +659,11 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
     reinterpret_cast<float4 *>(osum + h * D)[dq] = acc;
   }
   __syncthreads();
-  finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, arrivals, ws, out, lse,
-                         reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4));
+  if (in_cluster)
+    cluster_merge<NT, D, G>(orow0, osum, mfin, lfin, out, lse);
+  else
+    finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, arrivals, ws, out, lse,
+                           reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4));
 }
 
 // ===========================================================================
@@ -576,12 +686,12 @@ struct FfmaLayout {
   static_assert(2 * kStageBytes >= 3 * kMaxG * kAttnMaxSplits * 4, "merge scratch must fit in the V stages");
 };
 
-template <int D, int G, bool kStep>
+template <int D, int G>
 __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
                                 const bs_head_cfg &cfg, const int32_t *__restrict__ sel_idx,
                                 const int32_t *__restrict__ sel_cnt, int32_t *__restrict__ arrivals,
                                 float *__restrict__ ws, float *__restrict__ out, float *__restrict__ lse,
-                                int32_t *st, unsigned char *smem) {
+                                int32_t *st, unsigned char *smem, bool in_step, bool in_cluster) {
   using L = FfmaLayout<D, G>;
   constexpr int NT = kFfmaThreads;
   constexpr int DPL = D / 32;
@@ -596,13 +706,13 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  const UnitBlocks ub = load_unit_blocks<NT, kStep>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st);
+  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);
     return;
   }
-  if (split >= ub.pg.n_split) return;
-  const int gp0 = split * ub.pg.pps;
+  if (!in_cluster && split >= ub.pg.n_split) return;
+  const int gp0 = min(split * ub.pg.pps, ub.pg.n_pages);
   const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
   const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
   const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
@@ -637,7 +747,7 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   };
 
   if (warp == 0) {
-    issue(0, 0);
+    if (n_stages > 0) issue(0, 0);
     if (n_stages > 1) issue(1, 1);
   }
   {
@@ -657,7 +767,7 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   for (int it = 0; it < n_stages; ++it) {
     const int buf = it & 1;
     const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st);
-    if (__syncthreads_or(!ok)) return;
+    if (__syncthreads_or(!ok)) break;
 
     const unsigned char *Kb = smem + buf * L::kStageBytes;
     const bool tvalid = (tok & (kPage - 1)) < slot_valid[buf][tok >> 4];
@@ -766,8 +876,11 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
     osum[h * D + dd] = sum;
   }
   __syncthreads();
-  finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], arrivals, ws, out, lse,
-                         reinterpret_cast<float *>(smem + 2 * L::kStageBytes));
+  if (in_cluster)
+    cluster_merge<NT, D, G>(orow0, osum, ml_sm[0], ml_sm[1], out, lse);
+  else
+    finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], arrivals, ws, out, lse,
+                           reinterpret_cast<float *>(smem + 2 * L::kStageBytes));
 }
 
 }  // namespace bsi

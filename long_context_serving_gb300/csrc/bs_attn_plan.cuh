@@ -1,25 +1,34 @@
-// Split-KV plan of bs_sparse_decode_attn, shared by the split kernel, the merge
-// kernel and the workspace size.
+// Split-KV plan of the sparse decode attention, shared by the kernels and the host.
 #pragma once
 
 #include "bs_internal.cuh"
 
 namespace bsi {
 
-constexpr int kAttnThreads = 256;                  // 8 warps
 constexpr int kStagePages = 4;                     // pages staged per pipeline step
 constexpr int kStageTokens = kStagePages * kPage;  // 64 tokens
-constexpr int kAttnMaxSplits = 32;                 // splits per unit, at most
+constexpr int kClusterSplits = 16;                 // splits of a unit in one thread-block cluster
+constexpr int kClusterMaxPages = 1024;             // largest selection (pages) the cluster mode takes
+constexpr int kAttnMaxSplits = 32;                 // splits of a unit in the workspace mode
 
-// One partial record per (unit, split, head): o[D] (unnormalised), m (log2 units), l, 2 pad.
+// One partial record per (unit, split, head) in the workspace mode: o[D]
+// (unnormalised), m (log2 units), l, 2 pad.
 __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 
 // The workspace starts with two int32 arrival counters per unit (the selection phase
-// of the fused decode step, then the attention), padded to 16 bytes.
+// of the fused decode step, then the attention in workspace mode), padded to 16 bytes.
 __host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (2 * units + 3) / 4 * 4; }
 
-// Splits launched per unit: enough for the largest gathered page count.
+// Cluster mode: a unit's splits are the 16 CTAs of one cluster and merge through
+// distributed shared memory. Workspace mode (selections above 1024 pages): up to 32
+// splits per unit merge through records in the workspace.
+__host__ __device__ inline bool attn_cluster_mode(int max_gather_pages) {
+  return max_gather_pages <= kClusterMaxPages;
+}
+
+// Splits launched per unit.
 __host__ __device__ inline int attn_grid_splits(int max_gather_pages) {
+  if (attn_cluster_mode(max_gather_pages)) return kClusterSplits;
   int splits = (max_gather_pages + kStagePages - 1) / kStagePages;
   if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
   return splits < 1 ? 1 : splits;
@@ -30,11 +39,12 @@ __host__ __device__ inline int attn_grid_splits(int max_gather_pages) {
 struct UnitPages {
   int n_pages;   // gathered pages (0 when the unit has nothing to attend or is invalid)
   int ppb;       // pages per block
-  int pps;       // pages per split (a multiple of kStagePages)
+  int pps;       // pages per split
   int n_split;
 };
 
-__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk) {
+// The split plan depends only on the unit's own page count and the mode.
+__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk, bool cluster) {
   UnitPages p;
   p.ppb = g / kPage;
   p.n_pages = 0;
@@ -44,9 +54,13 @@ __device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_
   const int rem_pages = (T - last_blk * g + kPage - 1) / kPage;
   const int last_pages = rem_pages < p.ppb ? rem_pages : p.ppb;
   p.n_pages = (cnt - 1) * p.ppb + last_pages;
-  int per = (p.n_pages + kStagePages * kAttnMaxSplits - 1) / (kStagePages * kAttnMaxSplits);
-  if (per < 1) per = 1;
-  p.pps = kStagePages * per;
+  if (cluster) {
+    p.pps = (p.n_pages + kClusterSplits - 1) / kClusterSplits;
+  } else {
+    int per = (p.n_pages + kStagePages * kAttnMaxSplits - 1) / (kStagePages * kAttnMaxSplits);
+    if (per < 1) per = 1;
+    p.pps = kStagePages * per;
+  }
   p.n_split = (p.n_pages + p.pps - 1) / p.pps;
   return p;
 }

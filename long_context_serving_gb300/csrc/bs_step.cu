@@ -1,20 +1,22 @@
 // The fused decode step of one layer: all five steps of the path in two launches.
 //
-// Launch 1, step_front_kernel, one CTA per (score tile, unit):
-//   * every tile of a retrieval or dual unit scores its candidate blocks (a2);
+// Launch 1, step_front_kernel, one CTA per (unit, score tile), tile-major:
+//   * every tile of a retrieval or dual unit scores its candidate blocks (a2); tile 0
+//     also recomputes the sub-block holding the token just appended (a1). That
+//     sub-block lies in the always-forced tail block, which no score of this step
+//     reads, so a1 runs beside a2;
 //   * the last tile of each unit to finish (an integer arrival ticket, one acquire-
-//     release atomic per CTA) selects the unit's blocks (a3), writes the selection and
-//     its set-difference against the previous step (a5), and recomputes the sub-block
-//     holding the token just appended (a1). That sub-block lies in the always-forced
-//     tail block, which no score of this step reads, so a1 can follow a2;
-//   * a streaming unit has one tile that does the last three.
+//     release atomic per CTA) selects the unit's blocks (a3), publishes the selection
+//     (its count is written last, with a release store) and writes its set-difference
+//     against the previous step (a5);
+//   * a streaming unit has one tile that does a1, a3 and a5.
 // Launch 2, the attention (a4) as a programmatic dependent launch: streaming units'
-// splits need no selection and run while launch 1 is still working; the other splits
-// wait for launch 1 (griddepcontrol.wait) before reading their selection.
+// splits need no selection and start while launch 1 is still working; every other
+// unit's splits wait (bounded) until their unit's selection count is published.
 //
 // Both kernels are programmatic dependents of the work before them in the stream: they
 // read only the per-unit head configuration before waiting for it to finish.
-#include "bs_attn_impl.cuh"
+#include "bs_attn_launch.cuh"
 #include "bs_score_impl.cuh"
 #include "bs_select_impl.cuh"
 #include "bs_summaries_impl.cuh"
@@ -25,19 +27,33 @@ namespace {
 constexpr int kFrontThreads = 256;
 constexpr int kStepMaxSel = 4096;
 
-__host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel) {
-  const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
-  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4;
+__device__ __forceinline__ void pdl_wait_front() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger_front() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void store_release(int32_t *p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
 }
 
-template <int D, typename KT, int G>
+// Shared memory of the selection phase: keys [MB] u32, flags [MB] u8 (padded to 16),
+// current and previous selection [MS] i32 each, a bitmap of the previous one.
+__host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel) {
+  const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
+  const size_t words = (static_cast<size_t>(max_blocks) + 31) / 32;
+  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4 + words * 4;
+}
+
+template <int D, int G>
 __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
                                                                    bs_step_io io, int reduce, int32_t *arrivals) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t bar;
   __shared__ SelShared<kFrontThreads> sh;
   __shared__ int is_last;
-  const int u = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x;
+  const int u = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x;  // tile-major: every unit's tile 0 first
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const int MB = dims.max_blocks_per_unit, MS = dims.max_sel_per_unit;
   int32_t *st = io.dev_status;
@@ -46,8 +62,16 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   const int k = cfg.k_total[u], k_e = cfg.k_evict[u], sink = cfg.sink_tokens[u], local = cfg.local_tokens[u];
   const int64_t off = cfg.sum_off[u];
   const int rows = cfg.sum_rows[u];
-  pdl_wait();                // q, lengths, KV pages, summaries and selection state are now final
-  pdl_launch_dependents();   // the attention may start launching
+  pdl_wait_front();  // q, lengths, KV pages, summaries and selection state are now final
+  // The attention reads a non-streaming unit's selection once its count is >= 0: mark
+  // it not ready before any attention CTA can start (the buffer's last readers, the
+  // previous step, have finished).
+  if (tile == 0 && tid == 0) {
+    io.cur_cnt[u] = -1;
+    __threadfence();
+  }
+  __syncthreads();
+  pdl_trigger_front();  // the attention may start launching
 
   const int T = kv.seq_lens[b];
   const size_t srow = static_cast<size_t>(u) * MS;
@@ -60,13 +84,14 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   else if (off % 4 != 0) code = BS_ERR_ALIGN;
   if (code != BS_OK) {
     if (tile == 0) {
+      for (int i = tid; i < MS; i += kFrontThreads) io.cur_idx[srow + i] = io.added[srow + i] = io.removed[srow + i] = -1;
+      __syncthreads();
       if (tid == 0) {
         report(st, code);
-        io.cur_cnt[u] = 0;
         io.added_cnt[u] = 0;
         io.removed_cnt[u] = 0;
+        store_release(io.cur_cnt + u, 0);
       }
-      for (int i = tid; i < MS; i += kFrontThreads) io.cur_idx[srow + i] = io.added[srow + i] = io.removed[srow + i] = -1;
     }
     return;
   }
@@ -84,9 +109,21 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
     if (!score_tile<D, G>(io.summaries + off, qrow, dims.q_dtype, ge, tile, reduce, score_row, smem, &bar, st))
       return;
   }
+  // ---- a1: the sub-block holding the appended token (tile 0, beside the others) ----
+  if (tile == 0 && tid < 32) {
+    const int j = (T - 1) / s;
+    const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+    float *row = io.summaries + off + static_cast<int64_t>(j) * D;
+    const bool ok = dims.kv_dtype == BS_BF16
+                        ? summary_update_warp<D, uint16_t>(static_cast<const uint16_t *>(kv.k_pool), pt,
+                                                           dims.n_pages, s, T, j, row)
+                        : summary_update_warp<D, float>(static_cast<const float *>(kv.k_pool), pt, dims.n_pages,
+                                                        s, T, j, row);
+    if (!ok && tid == 0) report(st, BS_ERR_DEVICE_BOUNDS);
+  }
   if (n_tiles > 1) {
     __syncthreads();
-    if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == n_tiles - 1);
+    if (tid == 0) is_last = (ticket_acq_rel(arrivals + u) == n_tiles - 1);
     __syncthreads();
     if (!is_last) return;
   }
@@ -96,6 +133,17 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   uint8_t *flags = reinterpret_cast<uint8_t *>(keys + MB);
   int32_t *cur_sm = reinterpret_cast<int32_t *>(smem + static_cast<size_t>(MB) * 4 + ((MB + 15) & ~15));
   int32_t *prev_sm = cur_sm + MS;
+  uint32_t *pbits = reinterpret_cast<uint32_t *>(prev_sm + MS);
+  // The previous selection is final since the previous step: start its loads now into
+  // registers; they land while the selection runs.
+  constexpr int kPrevPer = kStepMaxSel / kFrontThreads;
+  const int np_raw = io.prev_cnt[u];
+  int32_t pv[kPrevPer];
+#pragma unroll
+  for (int j = 0; j < kPrevPer; ++j) {
+    const int i = tid + j * kFrontThreads;
+    pv[j] = i < MS ? io.prev_idx[srow + i] : -1;
+  }
   SelUnit su;
   su.cls = cls;
   su.k = k;
@@ -110,126 +158,74 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
     if (tid == 0) report(st, BS_ERR_CAPACITY);
     total = 0;
   }
-  if (tid == 0) io.cur_cnt[u] = total;
-
-  // ---- a5: set-difference against the previous selection --------------------------
-  int np = io.prev_cnt[u];
+  // Publish: the row is written; the count (release) tells the attention it is ready.
+  __syncthreads();
+  if (tid == 0) store_release(io.cur_cnt + u, total);
+  int np = np_raw;
   if (np < 0 || np > MS) {
     if (tid == 0) report(st, BS_ERR_CAPACITY);
     np = 0;
   }
-  for (int i = tid; i < np; i += kFrontThreads) prev_sm[i] = io.prev_idx[srow + i];
-  __syncthreads();
-  const int na = sorted_diff_into<kFrontThreads>(cur_sm, total, prev_sm, np, io.added + srow, MS, sh);
-  const int nr = sorted_diff_into<kFrontThreads>(prev_sm, np, cur_sm, total, io.removed + srow, MS, sh);
-  if (tid == 0) {
-    io.added_cnt[u] = na;
-    io.removed_cnt[u] = nr;
+#pragma unroll
+  for (int j = 0; j < kPrevPer; ++j) {
+    const int i = tid + j * kFrontThreads;
+    if (i < np) prev_sm[i] = pv[j];
   }
 
-  // ---- a1: the sub-block holding the appended token -------------------------------
-  if (tid < 32) {
-    const int j = (T - 1) / s;
-    const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
-    if (!summary_update_warp<D, KT>(static_cast<const KT *>(kv.k_pool), pt, dims.n_pages, s, T, j,
-                                    io.summaries + off + static_cast<int64_t>(j) * D) &&
-        tid == 0)
-      report(st, BS_ERR_DEVICE_BOUNDS);
+  // ---- a5: set-difference against the previous selection --------------------------
+  const int2 nd = setdiff_after_select<kFrontThreads>(cur_sm, total, prev_sm, np, flags, ge.n_blk, pbits,
+                                                      (MB + 31) / 32, io.added + srow, io.removed + srow, MS, sh);
+  if (tid == 0) {
+    io.added_cnt[u] = nd.x;
+    io.removed_cnt[u] = nd.y;
   }
   if (tid == 0 && n_tiles > 1) arrivals[u] = 0;  // ready for the next step
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kMmaThreads) step_attn_mma_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
-                                                                    const __grid_constant__ CUtensorMap tmk,
-                                                                    const __grid_constant__ CUtensorMap tmv,
-                                                                    bs_step_io io, int32_t *arrivals, float *records) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  pdl_launch_dependents();
-  attn_split_mma<D, G, true>(dims, io.q, kv, cfg, &tmk, &tmv, io.cur_idx, io.cur_cnt, arrivals, records, io.out,
-                             io.lse, io.dev_status, align_smem_1024(smem_raw));
-  // Finish only after the selection launch has: work after this step may rely on it.
-  pdl_wait();
-}
-
-template <int D, int G>
-__global__ void __launch_bounds__(kFfmaThreads) step_attn_ffma_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
-                                                                      bs_step_io io, int32_t *arrivals,
-                                                                      float *records) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  pdl_launch_dependents();
-  attn_split_ffma<D, G, true>(dims, io.q, kv, cfg, io.cur_idx, io.cur_cnt, arrivals, records, io.out, io.lse,
-                              io.dev_status, smem);
-  pdl_wait();
-}
-
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t cs, Args... args) {
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = grid;
-  lc.blockDim = dim3(threads);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = cs;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, kernel, args...);
-}
-
-template <int D, typename KT, int G>
 bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg, const bs_step_io &io,
                       int reduce, cudaStream_t cs) {
   constexpr size_t kFrontMaxSmem = 200 * 1024;
-  constexpr bool kBf16 = sizeof(KT) == 2;
-  constexpr int kAttnSmem = kBf16 ? MmaLayout<D>::kBytes + kSmemAlignSlack : FfmaLayout<D, G>::kBytes;
-  static const bool attrs_ok =
-      cudaFuncSetAttribute(step_front_kernel<D, KT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kFrontMaxSmem)) == cudaSuccess &&
-      (kBf16 ? cudaFuncSetAttribute(step_attn_mma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kAttnSmem)
-             : cudaFuncSetAttribute(step_attn_ffma_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kAttnSmem)) == cudaSuccess;
-  if (!attrs_ok) return BS_ERR_CUDA;
+  static const bool attr_ok = cudaFuncSetAttribute(step_front_kernel<D, G>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
+  if (!attr_ok) return BS_ERR_CUDA;
   const int units = dims.batch * dims.n_kv_heads;
   size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit);
   if (front_smem < static_cast<size_t>(ScoreLayout<D, G>::kBytes)) front_smem = ScoreLayout<D, G>::kBytes;
   if (front_smem > kFrontMaxSmem) return BS_ERR_CAPACITY;
-  CUtensorMap tk, tv;
-  if (kBf16) {
-    const bs_status s = make_kv_tensor_maps(dims, kv, &tk, &tv);
-    if (s != BS_OK) return s;
-  }
   int32_t *counters = static_cast<int32_t *>(io.workspace);
-  float *records = static_cast<float *>(io.workspace) + attn_counter_floats(units);
-  const dim3 front_grid(dims.max_subs_per_unit / kTileRows + 2, units);
-  if (launch_pdl(step_front_kernel<D, KT, G>, front_grid, kFrontThreads, front_smem, cs, dims, kv, cfg, io, reduce,
-                 counters) != cudaSuccess)
+  const dim3 front_grid(units, dims.max_subs_per_unit / kTileRows + 2);
+  if (launch_ex(step_front_kernel<D, G>, front_grid, kFrontThreads, front_smem, cs, 0, true, dims, kv, cfg, io,
+                reduce, counters) != cudaSuccess)
     return BS_ERR_CUDA;
-  const dim3 attn_grid(attn_grid_splits(dims.max_gather_pages_per_unit), units);
-  cudaError_t e;
-  if (kBf16)
-    e = launch_pdl(step_attn_mma_kernel<D, G>, attn_grid, kMmaThreads, static_cast<size_t>(kAttnSmem), cs, dims, kv,
-                   cfg, tk, tv, io, counters + units, records);
-  else
-    e = launch_pdl(step_attn_ffma_kernel<D, G>, attn_grid, kFfmaThreads, static_cast<size_t>(kAttnSmem), cs, dims,
-                   kv, cfg, io, counters + units, records);
-  return e == cudaSuccess ? BS_OK : BS_ERR_CUDA;
+  AttnArgs a;
+  a.dims = dims;
+  a.q = io.q;
+  a.kv = kv;
+  a.cfg = cfg;
+  a.sel_idx = io.cur_idx;
+  a.sel_cnt = io.cur_cnt;
+  a.out = io.out;
+  a.lse = io.lse;
+  a.arrivals = counters + units;
+  a.records = static_cast<float *>(io.workspace) + attn_counter_floats(units);
+  a.st = io.dev_status;
+  return dims.kv_dtype == BS_BF16 ? launch_attn_bf16(a, true, cs) : launch_attn_f32(a, true, cs);
 }
 
-template <int D, typename KT>
+template <int D>
 bs_status dispatch_g(int G, const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg, const bs_step_io &io,
                      int reduce, cudaStream_t cs) {
   switch (G) {
-    case 1: return launch_step<D, KT, 1>(dims, kv, cfg, io, reduce, cs);
-    case 2: return launch_step<D, KT, 2>(dims, kv, cfg, io, reduce, cs);
-    case 3: return launch_step<D, KT, 3>(dims, kv, cfg, io, reduce, cs);
-    case 4: return launch_step<D, KT, 4>(dims, kv, cfg, io, reduce, cs);
-    case 5: return launch_step<D, KT, 5>(dims, kv, cfg, io, reduce, cs);
-    case 6: return launch_step<D, KT, 6>(dims, kv, cfg, io, reduce, cs);
-    case 7: return launch_step<D, KT, 7>(dims, kv, cfg, io, reduce, cs);
-    default: return launch_step<D, KT, 8>(dims, kv, cfg, io, reduce, cs);
+    case 1: return launch_step<D, 1>(dims, kv, cfg, io, reduce, cs);
+    case 2: return launch_step<D, 2>(dims, kv, cfg, io, reduce, cs);
+    case 3: return launch_step<D, 3>(dims, kv, cfg, io, reduce, cs);
+    case 4: return launch_step<D, 4>(dims, kv, cfg, io, reduce, cs);
+    case 5: return launch_step<D, 5>(dims, kv, cfg, io, reduce, cs);
+    case 6: return launch_step<D, 6>(dims, kv, cfg, io, reduce, cs);
+    case 7: return launch_step<D, 7>(dims, kv, cfg, io, reduce, cs);
+    default: return launch_step<D, 8>(dims, kv, cfg, io, reduce, cs);
   }
 }
 
@@ -256,10 +252,6 @@ extern "C" bs_status bs_decode_step(const bs_dims *dims, const bs_kv *kv, const 
   if (dims->max_sel_per_unit > kStepMaxSel) return BS_ERR_CAPACITY;
   const int G = dims->n_q_heads / dims->n_kv_heads;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (dims->head_dim == 128) {
-    if (dims->kv_dtype == BS_BF16) return dispatch_g<128, uint16_t>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
-    return dispatch_g<128, float>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
-  }
-  if (dims->kv_dtype == BS_BF16) return dispatch_g<64, uint16_t>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
-  return dispatch_g<64, float>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
+  if (dims->head_dim == 128) return dispatch_g<128>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
+  return dispatch_g<64>(G, *dims, *kv, *cfg, *io, group_reduce, cs);
 }

@@ -78,6 +78,15 @@ def test_fused_step_matches_separate_calls():
     assert a.read_status() == 0 and b.read_status() == 0
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_large_selection_workspace_merge(fused):
+    """Selections above 1024 pages per unit merge their splits through the workspace."""
+    wl = make_workload(2, seed=14, T=20000)
+    wl.k[4:] = 600                      # ~1200 pages per retrieval unit
+    rep = run_parity(wl, fused=fused)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
