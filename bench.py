@@ -182,20 +182,24 @@ def algorithmic_bytes(wl, sel_lists, prev_lists):
     return out
 
 
-def _source_sha(path: str) -> str:
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+def csrc_sha() -> str:
+    """Hash of every CUDA source and header of the library (any change invalidates counters)."""
+    d = os.path.join(ROOT, "long_context_serving_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
 
 
-def _measured_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def _measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if no kernel source changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(kernel)
-    if not rec:
-        return None
-    src = os.path.join(ROOT, "long_context_serving_gb300", "csrc", rec["source"])
-    if not os.path.exists(src) or _source_sha(src) != rec["source_sha"]:
+    if not rec or rec.get("workload") != workload or rec.get("csrc_sha") != csrc_sha():
         return None
     return rec["bytes_per_launch"]
 
@@ -216,6 +220,17 @@ def _peak_hbm():
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+def max_over_ranks(x: float, device) -> float:
+    """The largest of every rank's x (a time); x itself on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_ours(args) -> None:
     import numpy as np
     import torch
@@ -305,10 +320,7 @@ def run_ours(args) -> None:
     for i in range(args.warmup):
         graphs[i % 2].replay()
     ms = timed_replays(graphs, args.steps)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     soak_s = 0.0
     while soak_s < 1.0 - ms / 1000:
         t0 = time.perf_counter()
@@ -347,8 +359,9 @@ def run_ours(args) -> None:
     dominant = max(("attn", "score"), key=lambda k: per_kernel[k])
     peak, peak_note = _peak_hbm()
     achieved = nbytes[dominant] / (per_kernel[dominant] * 1e-6) / 1e9
-    kernel_name = {"attn": "attn_split_kernel", "score": "score_kernel"}[dominant]
-    traffic = _measured_traffic(kernel_name)
+    attn_kernel = "attn_mma_kernel" if wl.dtype == "bf16" else "attn_ffma_kernel"
+    kernel_name = {"attn": attn_kernel, "score": "score_kernel"}[dominant]
+    traffic = _measured_traffic(kernel_name, "llama8b-32k")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel_name,
                 "peak_source": peak_note, "algorithmic_bytes_per_launch": nbytes[dominant],
@@ -381,10 +394,7 @@ def run_ours(args) -> None:
     for i in range(args.steps):
         e2e_step(i)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = e2e_s / args.steps * 1e6 / LAYERS
 
     cpu = None
@@ -398,7 +408,7 @@ def run_ours(args) -> None:
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": _config({"ranks": world, "parallelism": f"replicas x{world}, units independent",
                                    "path": args.path,
-                                   "graph": f"CUDA graph of 32 layers x {launches_per_step // LAYERS} launches"}),
+                                   "graph": f"CUDA graph of {LAYERS} layers x {launches_per_step // LAYERS} launches"}),
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},

@@ -163,9 +163,11 @@ __device__ __noinline__ void topk_mark_radix(const uint32_t *keys, uint8_t *flag
 // (keys[c - lo]), lower index first among equal keys; the same result as
 // topk_mark_radix with fewer CTA barriers:
 //   1. min, max and count of the eligible keys (one barrier);
-//   2. a histogram of (key - min) >> shift over 2048 buckets, shift chosen so that
-//      the key range fits; the bucket map is monotone, so every key in a bucket above
-//      the boundary bucket B is taken and every key below is not;
+//   2. a histogram over 2048 buckets of the float value placed linearly between the
+//      minimum and the maximum, (x - min) * (2048 / (max - min)) in fp32 with round to
+//      nearest: subtraction, multiplication by a positive constant and truncation are
+//      each monotone, so every key in a bucket above the boundary bucket B is taken
+//      and every key below is not;
 //   3. a suffix count over the buckets finds B and how many of its keys are taken;
 //   4. keys in B are ranked exactly by (key desc, index asc): directly when B holds
 //      at most 256 keys, otherwise by the radix select restricted to B.
@@ -217,11 +219,19 @@ __device__ __noinline__ void topk_mark(const uint32_t *keys, uint8_t *flags, int
     return;
   }
   // 2. histogram of the monotone bucket map
-  const uint32_t range = kmax - kmin;
-  const int bits = 32 - __clz(range);
-  const int shift = bits > 11 ? bits - 11 : 0;
+  // A zero, infinite or NaN range (equal keys, infinities) puts every key in bucket 0,
+  // which the exact rank below still orders correctly.
+  const float xmin = key_value(kmin);
+  const float range = key_value(kmax) - xmin;
+  float bscale = (range > 0.0f && range <= 3.0e38f) ? static_cast<float>(kBuckets) / range : 0.0f;
+  if (!(bscale <= 3.0e38f)) bscale = 0.0f;  // a subnormal range
+  auto bucket = [&](uint32_t key) -> uint32_t {
+    if (bscale == 0.0f) return 0u;
+    const float f = (key_value(key) - xmin) * bscale;  // in [0, 2048 (1 + eps)]
+    return f >= static_cast<float>(kBuckets - 1) ? static_cast<uint32_t>(kBuckets - 1) : static_cast<uint32_t>(f);
+  };
   for (int c = a; c < e; ++c)
-    if (flags[c] & kElig) atomicAdd(&sh.hist[(keys[c - lo] - kmin) >> shift], 1u);
+    if (flags[c] & kElig) atomicAdd(&sh.hist[bucket(keys[c - lo])], 1u);
   __syncthreads();
   // 3. thread t owns buckets [kBuckets - bpt (t + 1), kBuckets - bpt t): suffix counts
   constexpr int bpt = kBuckets / NT;
@@ -250,7 +260,7 @@ __device__ __noinline__ void topk_mark(const uint32_t *keys, uint8_t *flags, int
   // 4. take the buckets above B; collect B
   for (int c = a; c < e; ++c) {
     if (!(flags[c] & kElig)) continue;
-    const uint32_t bk = (keys[c - lo] - kmin) >> shift;
+    const uint32_t bk = bucket(keys[c - lo]);
     if (bk > B) flags[c] |= mark;
     else if (bk == B) {
       if (in_b <= kBndDirect) sh.bnd_idx[atomicAdd(&sh.bnd_n, 1)] = c;

@@ -40,6 +40,12 @@ __device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
 
 // Shared memory of the selection phase: keys [MB] u32, flags [MB] u8 (padded to 16),
 // current and previous selection [MS] i32 each, a bitmap of the previous one.
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel) {
   const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
   const size_t words = (static_cast<size_t>(max_blocks) + 31) / 32;
@@ -134,16 +140,12 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   int32_t *cur_sm = reinterpret_cast<int32_t *>(smem + static_cast<size_t>(MB) * 4 + ((MB + 15) & ~15));
   int32_t *prev_sm = cur_sm + MS;
   uint32_t *pbits = reinterpret_cast<uint32_t *>(prev_sm + MS);
-  // The previous selection is final since the previous step: start its loads now into
-  // registers; they land while the selection runs.
-  constexpr int kPrevPer = kStepMaxSel / kFrontThreads;
-  const int np_raw = io.prev_cnt[u];
-  int32_t pv[kPrevPer];
-#pragma unroll
-  for (int j = 0; j < kPrevPer; ++j) {
-    const int i = tid + j * kFrontThreads;
-    pv[j] = i < MS ? io.prev_idx[srow + i] : -1;
-  }
+  // The previous selection is final since the previous step: copy it asynchronously
+  // (cp.async) into shared memory; it lands while the selection runs.
+  __shared__ int np_sm;
+  if (tid == 0) cp_async4(&np_sm, io.prev_cnt + u);
+  for (int i = tid; i < MS; i += kFrontThreads) cp_async4(prev_sm + i, io.prev_idx + srow + i);
+  cp_async_commit();
   SelUnit su;
   su.cls = cls;
   su.k = k;
@@ -161,15 +163,12 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   // Publish: the row is written; the count (release) tells the attention it is ready.
   __syncthreads();
   if (tid == 0) store_release(io.cur_cnt + u, total);
-  int np = np_raw;
+  cp_async_wait_all();
+  __syncthreads();
+  int np = np_sm;
   if (np < 0 || np > MS) {
     if (tid == 0) report(st, BS_ERR_CAPACITY);
     np = 0;
-  }
-#pragma unroll
-  for (int j = 0; j < kPrevPer; ++j) {
-    const int i = tid + j * kFrontThreads;
-    if (i < np) prev_sm[i] = pv[j];
   }
 
   // ---- a5: set-difference against the previous selection --------------------------
