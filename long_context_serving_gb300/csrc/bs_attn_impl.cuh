@@ -54,11 +54,12 @@ constexpr int kMmaThreads = 128;  // bf16 path: 4 warps, one page each per stage
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ int load_acquire_gpu(const int32_t *p) {
+__device__ __forceinline__ int load_relaxed_gpu(const int32_t *p) {
   int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *p, int v) {
   int old;
@@ -114,11 +115,14 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
       int c = 0;
       if (in_step) {
         // The selection kernel publishes this unit's count with a release store once
-        // the row is written (-1 until then). Bounded wait: about one second.
-        c = load_acquire_gpu(sel_cnt + u);
+        // the row is written (-1 until then). Poll with relaxed loads and a short sleep
+        // (acquire loads in a tight loop slow down the other CTAs of the SM), then one
+        // acquire fence. Bounded wait: about one second.
+        c = load_relaxed_gpu(sel_cnt + u);
         if (c < 0) {
           const uint64_t t0 = global_ns();
-          while ((c = load_acquire_gpu(sel_cnt + u)) < 0) {
+          while ((c = load_relaxed_gpu(sel_cnt + u)) < 0) {
+            __nanosleep(64);
             if (global_ns() - t0 > 1000000000ull) {
               report(st, BS_ERR_TIMEOUT);
               c = 0;
@@ -126,6 +130,7 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
             }
           }
         }
+        fence_acq_rel_gpu();
       } else {
         c = sel_cnt[u];
       }

@@ -34,39 +34,53 @@ __host__ __device__ __forceinline__ int score_tiles(const Geom &ge) {
   return (ge.c_hi - ge.c_lo + bpt - 1) / bpt;
 }
 
-// Scores tile `tile` of a unit's candidates into row_out[c] (c = block index).
-// summ_unit points at the unit's first summary row (16-byte aligned); qrow at its G
-// query vectors. Returns false when the bulk copy timed out. All 256 threads call it
-// with the same arguments; the tile must exist.
+// Starts the bulk copy of summary rows [row0, min(row0 + 64, row_end)) of a unit
+// (summ_unit: its first row, 16-byte aligned) into the tile buffer and returns the row
+// count (0: nothing in flight). The barrier is initialised either way; every thread
+// calls it, and every thread must call score_tile_finish afterwards, which waits for
+// the copy, before the shared memory is reused or the CTA exits.
 template <int D, int G>
-__device__ bool score_tile(const float *summ_unit, const void *qrow, int q_dtype, const Geom &ge, int tile,
-                           int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
+__device__ __forceinline__ int score_tile_issue(const float *summ_unit, int64_t row0, int64_t row_end,
+                                                unsigned char *smem, uint64_t *bar) {
+  const int64_t left = row_end - row0;
+  const int n = row0 < 0 ? 0 : static_cast<int>(left < kTileRows ? (left > 0 ? left : 0) : kTileRows);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    if (n > 0) {
+      const uint32_t bytes = static_cast<uint32_t>(n) * D * sizeof(float);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(smem, summ_unit + row0 * D, bytes, bar);
+    }
+  }
+  __syncthreads();
+  return n;
+}
+
+// Waits for the copy started by score_tile_issue (n_loaded rows) and, if `score`,
+// scores tile `tile` of the unit's candidates into row_out[c] (c = block index): the
+// copied rows must start at row c_lo * r + 64 * tile and cover the tile. qrow points at
+// the unit's G query vectors. Returns false when the copy timed out. All 256 threads
+// call it with the same arguments.
+template <int D, int G>
+__device__ bool score_tile_finish(int n_loaded, bool score, const void *qrow, int q_dtype, const Geom &ge, int tile,
+                                  int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
   using L = ScoreLayout<D, G>;
   float *tile_sm = reinterpret_cast<float *>(smem);          // [64][D]
   float *qs = reinterpret_cast<float *>(smem + L::kOffQ);     // [G][D]
   float *dots = reinterpret_cast<float *>(smem + L::kOffDots);  // [64][G]
   const int tid = threadIdx.x;
+  const float scale = rsqrtf(static_cast<float>(D));
+  if (score)
+    for (int i = tid; i < G * D; i += kScoreThreads) qs[i] = load_scalar(qrow, i, q_dtype) * scale;
+  const bool ok = n_loaded == 0 || mbar_wait_bounded(bar, 0, st);
+  if (__syncthreads_or(!ok)) return false;
+  if (!score) return true;
   const int r = ge.g / ge.s;
   const int bpt = kTileRows / r;
   const int c_first = ge.c_lo + tile * bpt;
   const int nb = min(bpt, ge.c_hi - c_first);
-  const int nrows = nb * r;
-  const int64_t row0 = static_cast<int64_t>(c_first) * r;
-
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t bytes = static_cast<uint32_t>(nrows) * D * sizeof(float);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(tile_sm, summ_unit + row0 * D, bytes, bar);
-  }
-  const float scale = rsqrtf(static_cast<float>(D));
-  for (int i = tid; i < G * D; i += kScoreThreads) qs[i] = load_scalar(qrow, i, q_dtype) * scale;
-  const bool ok = mbar_wait_bounded(bar, 0, st);
-  if (__syncthreads_or(!ok)) return false;
+  const int nrows = min(nb * r, n_loaded);
 
   // Dot products: thread (row, quarter).
   constexpr int kChunks = D / 4;     // float4 chunks per row
@@ -114,6 +128,22 @@ __device__ bool score_tile(const float *summ_unit, const void *qrow, int q_dtype
     row_out[c_first + tid] = red;
   }
   return true;
+}
+
+// Scores tile `tile` of a unit's candidates into row_out[c] (c = block index).
+// summ_unit points at the unit's first summary row (16-byte aligned); qrow at its G
+// query vectors. Returns false when the bulk copy timed out. All 256 threads call it
+// with the same arguments; the tile must exist.
+template <int D, int G>
+__device__ bool score_tile(const float *summ_unit, const void *qrow, int q_dtype, const Geom &ge, int tile,
+                           int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
+  const int r = ge.g / ge.s;
+  const int bpt = kTileRows / r;
+  const int c_first = ge.c_lo + tile * bpt;
+  const int nb = min(bpt, ge.c_hi - c_first);
+  const int64_t row0 = static_cast<int64_t>(c_first) * r;
+  const int n = score_tile_issue<D, G>(summ_unit, row0, row0 + nb * r, smem, bar);
+  return score_tile_finish<D, G>(n, true, qrow, q_dtype, ge, tile, reduce, row_out, smem, bar, st);
 }
 
 }  // namespace bsi

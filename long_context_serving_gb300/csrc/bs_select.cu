@@ -1,5 +1,5 @@
 // a3: per-unit block selection, stand-alone kernel (one CTA of 512 threads per unit).
-// The selection itself is select_unit_flags() in bs_select_impl.cuh.
+// The selection itself is select_unit() in bs_select_impl.cuh.
 #include "bs_select_impl.cuh"
 
 namespace bsi {
@@ -46,8 +46,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(bs_dims dims, bs_he
   su.scores = scores + row;
   su.evict = cls == BS_DUAL ? evict + row : nullptr;
   su.alive = cls == BS_DUAL ? alive + row : nullptr;
-  select_unit_flags<kSelThreads>(su, keys, flags, sh);
-  const int total = compact_selection<kSelThreads>(flags, su.ge.n_blk, out, dims.max_sel_per_unit, nullptr, sh);
+  const int total = select_unit<kSelThreads>(su, keys, flags, out, dims.max_sel_per_unit, nullptr, sh);
   if (tid == 0) {
     if (total < 0) report(st, BS_ERR_CAPACITY);
     sel_cnt[u] = total < 0 ? 0 : total;

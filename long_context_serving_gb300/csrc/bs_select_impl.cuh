@@ -32,12 +32,25 @@ struct SelShared {
   static constexpr int kWarps = NT / 32;
   uint32_t hist[kBuckets];      // the radix passes use the first 256
   int warp_tot[kWarps];
+  int wt[2][kWarps];            // warp totals of the one-barrier scan, two buffers
   uint32_t warp_min[kWarps], warp_max[kWarps];
   int warp_cnt[kWarps];
   int bcast[4];
   int bnd_n;
   int bnd_idx[kBndDirect];
+  int ord[NT];                  // per (round, warp) counts of the ordered ranking
+  int ord2[NT];                 // their exclusive prefix
 };
+
+__device__ __forceinline__ bool sorted_contains(const int32_t *v, int n, int x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] < x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo < n && v[lo] == x;
+}
 
 // Exclusive prefix sum of one int per thread over the CTA; *total gets the sum.
 template <int NT>
@@ -368,6 +381,320 @@ __device__ __noinline__ int compact_selection(const uint8_t *flags, int n_blk, i
 }
 
 // ---------------------------------------------------------------------------
+// Register-resident selection (units with at most NT * R candidates).
+//
+// Candidate c = c_lo + i * NT + t is element i of thread t: the loads of scores and
+// logits are coalesced, every per-candidate decision is a bit of a per-thread mask,
+// and shared memory holds only a histogram and a few reduction slots. The top-k refines
+// a 2048-bucket histogram level by level (linear float buckets first, then integer
+// buckets on the order keys, each level shrinking the key range of the boundary bucket
+// by 2^11) until the boundary bucket is taken whole or all its keys are equal; equal
+// keys go to the lowest block index. The output order is ascending block index: a
+// ranking of the taken candidates by ballots per (round, warp) and one prefix scan.
+// ---------------------------------------------------------------------------
+
+// Exclusive prefix sum over the CTA with one barrier. Two consecutive calls with the
+// same `buf` need a barrier between them. *total gets the sum.
+template <int NT>
+__device__ __forceinline__ int block_scan1(int v, SelShared<NT> &sh, int buf, int *total) {
+  constexpr int W = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh.wt[buf][warp] = x;
+  __syncthreads();
+  int off = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const int t = sh.wt[buf][w];
+    off += w < warp ? t : 0;
+    tot += t;
+  }
+  *total = tot;
+  return off + x - v;
+}
+
+// CTA-wide min, max and sum with one barrier (results in every thread).
+template <int NT>
+__device__ __forceinline__ void block_min_max_count(uint32_t &kmin, uint32_t &kmax, int &cnt, SelShared<NT> &sh) {
+  constexpr int W = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  }
+  if (lane == 0) {
+    sh.warp_min[warp] = kmin;
+    sh.warp_max[warp] = kmax;
+    sh.warp_cnt[warp] = cnt;
+  }
+  __syncthreads();
+  kmin = 0xffffffffu;
+  kmax = 0u;
+  cnt = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    kmin = min(kmin, sh.warp_min[w]);
+    kmax = max(kmax, sh.warp_max[w]);
+    cnt += sh.warp_cnt[w];
+  }
+}
+
+// Rank of each set bit of `bits` among the set bits of the whole CTA in ascending
+// candidate order (rank[i] is valid where bit i is set). Returns the number of set bits.
+template <int NT, int R>
+__device__ __forceinline__ int ordered_ranks(uint32_t bits, int nr, int (&rank)[R], SelShared<NT> &sh) {
+  constexpr int W = NT / 32;
+  static_assert(R * W <= NT, "one scan slot per (round, warp)");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    rank[i] = 0;
+    if (i < nr) {
+      const uint32_t m = __ballot_sync(0xffffffffu, (bits >> i) & 1u);
+      rank[i] = __popc(m & lt);
+      if (lane == 0) sh.ord[i * W + warp] = __popc(m);
+    }
+  }
+  __syncthreads();
+  int total;
+  const int ex = block_scan1<NT>(threadIdx.x < nr * W ? sh.ord[threadIdx.x] : 0, sh, 0, &total);
+  sh.ord2[threadIdx.x] = ex;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    if (i < nr) rank[i] += sh.ord2[i * W + warp];
+  return total;
+}
+
+// The k largest keys among the elements flagged in `elig` (lowest candidate index
+// first among equal keys); returns them as a mask. All threads call it with the same
+// nr and k.
+template <int NT, int R>
+__device__ __forceinline__ uint32_t topk_regs(const uint32_t (&key)[R], uint32_t elig, int nr, int k,
+                                              SelShared<NT> &sh) {
+  constexpr int bpt = kBuckets / NT;  // buckets per thread in the boundary search
+  const int tid = threadIdx.x;
+  uint32_t take = 0u, E = elig;
+  int need = k;
+  bool done = need <= 0;
+  __syncthreads();  // earlier readers of the reduction slots and the histogram are done
+  for (int level = 0; level < 6 && !done; ++level) {
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (i < nr && ((E >> i) & 1u)) {
+        kmin = min(kmin, key[i]);
+        kmax = max(kmax, key[i]);
+        ++cnt;
+      }
+    for (int j = tid; j < kBuckets; j += NT) sh.hist[j] = 0u;
+    block_min_max_count<NT>(kmin, kmax, cnt, sh);
+    if (need >= cnt) {
+      take |= E;
+      done = true;
+      break;
+    }
+    if (kmin == kmax) break;  // all equal: lowest indices, below
+    // Monotone bucket map: linear in the float value on the first level when the
+    // range is finite and normal, otherwise (key - kmin) >> shift.
+    const float xmin = key_value(kmin);
+    const float range = key_value(kmax) - xmin;
+    float bscale = (level == 0 && range > 0.0f && range <= 3.0e38f) ? static_cast<float>(kBuckets) / range : 0.0f;
+    if (!(bscale <= 3.0e38f)) bscale = 0.0f;
+    const uint32_t span = kmax - kmin;
+    const int bits = 32 - __clz(span);
+    const int shift = bits > 11 ? bits - 11 : 0;
+    auto bucket = [&](uint32_t kk) -> uint32_t {
+      if (bscale > 0.0f) {
+        const float f = (key_value(kk) - xmin) * bscale;  // in [0, 2048 (1 + eps)]
+        return f >= static_cast<float>(kBuckets - 1) ? static_cast<uint32_t>(kBuckets - 1) : static_cast<uint32_t>(f);
+      }
+      return (kk - kmin) >> shift;
+    };
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (i < nr && ((E >> i) & 1u)) atomicAdd(&sh.hist[bucket(key[i])], 1u);
+    __syncthreads();
+    // Thread t owns buckets [kBuckets - bpt (t + 1), kBuckets - bpt t), highest first.
+    const int top = kBuckets - bpt * tid - 1;
+    int hc[bpt];
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < bpt; ++j) {
+      hc[j] = static_cast<int>(sh.hist[top - j]);
+      mine += hc[j];
+    }
+    int tot;
+    const int above = block_scan1<NT>(mine, sh, level & 1, &tot);
+    if (above < need && need <= above + mine) {
+      int run = above;
+#pragma unroll
+      for (int j = 0; j < bpt; ++j) {
+        if (run + hc[j] >= need) {
+          sh.bcast[0] = top - j;    // boundary bucket
+          sh.bcast[1] = need - run; // keys of it to take
+          sh.bcast[2] = hc[j];      // keys in it
+          break;
+        }
+        run += hc[j];
+      }
+    }
+    __syncthreads();
+    const uint32_t B = static_cast<uint32_t>(sh.bcast[0]);
+    const int rem = sh.bcast[1], in_b = sh.bcast[2];
+    uint32_t nextE = 0u;
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (i < nr && ((E >> i) & 1u)) {
+        const uint32_t bk = bucket(key[i]);
+        if (bk > B) take |= 1u << i;
+        else if (bk == B) nextE |= 1u << i;
+      }
+    E = nextE;
+    need = rem;
+    if (rem == in_b) {
+      take |= E;
+      done = true;
+    }
+  }
+  if (!done) {
+    // Every remaining key is equal (or the level bound was reached): take the `need`
+    // lowest candidate indices of E.
+    int rank[R];
+    ordered_ranks<NT, R>(E, nr, rank, sh);
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      if (i < nr && ((E >> i) & 1u) && rank[i] < need) take |= 1u << i;
+  }
+  return take;
+}
+
+// Selects the blocks of one unit (at most NT * R candidates) and writes them ascending
+// to out[0, cap) (-1 padded) and, if given, to `copy`. Dual units also update their
+// alive row. Returns the count, or -1 when it exceeds cap (the row is then all -1).
+// Reads scores with L2-only loads so that values written by other CTAs of the same grid
+// are seen. All NT threads call it.
+template <int NT, int R>
+__device__ __forceinline__ int select_unit_regs(const SelUnit &su, int32_t *out, int cap, int32_t *copy,
+                                                SelShared<NT> &sh) {
+  const int tid = threadIdx.x;
+  const Geom ge = su.ge;
+  const int lo = ge.c_lo, hi = ge.c_hi;
+  const int nr = (hi - lo + NT - 1) / NT;
+  uint32_t valid = 0u;
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    if (i < nr && lo + i * NT + tid < hi) valid |= 1u << i;
+  uint32_t take = 0u;
+  const int passes = su.cls == BS_DUAL ? 2 : (su.cls == BS_RETRIEVAL ? 1 : 0);
+  for (int p = 0; p < passes; ++p) {
+    // Dual: pass 0 is Gamma_e on the eviction logits among alive candidates; pass 1 is
+    // Gamma_q on the scores among the candidates outside Gamma_e. Retrieval: scores.
+    const bool gamma_e = su.cls == BS_DUAL && p == 0;
+    uint32_t key[R];
+    uint32_t elig = 0u;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      key[i] = 0u;
+      if ((valid >> i) & 1u) {
+        const int c = lo + i * NT + tid;
+        if (gamma_e) {
+          key[i] = order_key(su.evict[c]);
+          if (su.alive[c]) elig |= 1u << i;
+        } else {
+          key[i] = order_key(__ldcg(su.scores + c));
+          if (!((take >> i) & 1u)) elig |= 1u << i;
+        }
+      }
+    }
+    const int kk = gamma_e ? su.k_e : (su.cls == BS_DUAL ? su.k - su.k_e : su.k);
+    const uint32_t t = topk_regs<NT, R>(key, elig, nr, kk, sh);
+    if (gamma_e) {
+      // Strict eviction: candidates outside Gamma_e are dead from now on.
+#pragma unroll
+      for (int i = 0; i < R; ++i)
+        if ((valid >> i) & 1u) su.alive[lo + i * NT + tid] = static_cast<uint8_t>((t >> i) & 1u);
+    }
+    take |= t;
+  }
+  // Ascending output: sink blocks [0, c_lo), the taken candidates, local blocks [c_hi, n_blk).
+  int rank[R];
+  const int n_take = passes > 0 ? ordered_ranks<NT, R>(take, nr, rank, sh) : 0;
+  const int n_local = ge.n_blk - hi;
+  const int total = lo + n_take + n_local;
+  if (total > cap) {
+    for (int i = tid; i < cap; i += NT) out[i] = -1;
+    return -1;
+  }
+  for (int c = tid; c < lo; c += NT) {
+    out[c] = c;
+    if (copy) copy[c] = c;
+  }
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+    if ((take >> i) & 1u) {
+      const int pos = lo + rank[i], c = lo + i * NT + tid;
+      out[pos] = c;
+      if (copy) copy[pos] = c;
+    }
+  for (int j = tid; j < n_local; j += NT) {
+    const int pos = lo + n_take + j;
+    out[pos] = hi + j;
+    if (copy) copy[pos] = hi + j;
+  }
+  for (int i = total + tid; i < cap; i += NT) out[i] = -1;
+  return total;
+}
+
+// Selection of one unit into out[0, cap) (and `copy`): the register-resident path up
+// to NT * 32 candidates, otherwise flags and keys in shared memory (keys[n_blk],
+// flags[n_blk]). Returns the count, or -1 when it exceeds cap.
+template <int NT>
+__device__ __forceinline__ int select_unit(const SelUnit &su, uint32_t *keys, uint8_t *flags, int32_t *out, int cap,
+                                           int32_t *copy, SelShared<NT> &sh) {
+  const int nr = (su.ge.c_hi - su.ge.c_lo + NT - 1) / NT;
+  if (nr <= 4) return select_unit_regs<NT, 4>(su, out, cap, copy, sh);
+  if (nr <= 32) return select_unit_regs<NT, 32>(su, out, cap, copy, sh);
+  select_unit_flags<NT>(su, keys, flags, sh);
+  return compact_selection<NT>(flags, su.ge.n_blk, out, cap, copy, sh);
+}
+
+// Set-difference of two ascending lists in shared memory (cur[0, nc), prev[0, np)):
+// added = cur \ prev and removed = prev \ cur, ascending, -1 padded to cap. Membership by
+// binary search; one packed scan orders both outputs. All NT threads call it.
+template <int NT>
+__device__ __forceinline__ int2 setdiff_sorted(const int32_t *cur, int nc, const int32_t *prev, int np,
+                                               int32_t *added, int32_t *removed, int cap, SelShared<NT> &sh) {
+  const int tid = threadIdx.x;
+  const int pc = (nc + NT - 1) / NT, pp = (np + NT - 1) / NT;
+  const int ca = tid * pc, ce = min(nc, ca + pc);
+  const int pa = tid * pp, pe = min(np, pa + pp);
+  int na = 0, nr = 0;
+  for (int i = ca; i < ce; ++i) na += sorted_contains(prev, np, cur[i]) ? 0 : 1;
+  for (int i = pa; i < pe; ++i) nr += sorted_contains(cur, nc, prev[i]) ? 0 : 1;
+  int total;
+  const int packed = block_scan1<NT>((na << 16) | nr, sh, 1, &total);
+  int wa = packed >> 16, wr = packed & 0xffff;
+  for (int i = ca; i < ce; ++i)
+    if (!sorted_contains(prev, np, cur[i])) added[wa++] = cur[i];
+  for (int i = pa; i < pe; ++i)
+    if (!sorted_contains(cur, nc, prev[i])) removed[wr++] = prev[i];
+  const int ta = total >> 16, tr = total & 0xffff;
+  for (int i = ta + tid; i < cap; i += NT) added[i] = -1;
+  for (int i = tr + tid; i < cap; i += NT) removed[i] = -1;
+  return make_int2(ta, tr);
+}
+
+// ---------------------------------------------------------------------------
 // Set-difference of the new selection against the previous one, right after a
 // selection: membership of a previous block in the new selection is its kSel flag;
 // membership of a new block in the previous selection is a bit of `pbits` (one bit
@@ -419,15 +746,6 @@ __device__ __noinline__ int2 setdiff_after_select(const int32_t *cur, int nc, co
 // ---------------------------------------------------------------------------
 // Set-difference of two ascending lists held in shared memory.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool sorted_contains(const int32_t *v, int n, int x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (v[mid] < x) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo < n && v[lo] == x;
-}
 
 // Writes the elements of a[0..na) missing from b[0..nb) to dst (ascending), pads
 // with -1 up to cap and returns the count. All NT threads must call it.

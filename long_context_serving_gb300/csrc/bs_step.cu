@@ -38,8 +38,9 @@ __device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
   return old;
 }
 
-// Shared memory of the selection phase: keys [MB] u32, flags [MB] u8 (padded to 16),
-// current and previous selection [MS] i32 each, a bitmap of the previous one.
+// Shared memory of the selection phase: keys [MB] u32 and flags [MB] u8 (padded to
+// 16; used by selections above 32 candidates per thread), current and previous
+// selection [MS] i32 each.
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -48,12 +49,11 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel) {
   const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
-  const size_t words = (static_cast<size_t>(max_blocks) + 31) / 32;
-  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4 + words * 4;
+  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4;
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
+__global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
                                                                    bs_step_io io, int reduce, int32_t *arrivals) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t bar;
@@ -68,6 +68,14 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   const int k = cfg.k_total[u], k_e = cfg.k_evict[u], sink = cfg.sink_tokens[u], local = cfg.local_tokens[u];
   const int64_t off = cfg.sum_off[u];
   const int rows = cfg.sum_rows[u];
+  const bool cfg_ok = unit_cfg_ok(cls, g, s, k, k_e, sink, local);
+  const bool scored = cfg_ok && cls != BS_STREAMING;
+  // First summary row of this tile: candidates start after the sink blocks (the checks
+  // below confirm this once the length is known; otherwise the unit has no candidates).
+  const int64_t row0 =
+      scored ? static_cast<int64_t>((sink + g - 1) / g) * (g / s) + static_cast<int64_t>(tile) * kTileRows : -1;
+  // CTAs past every tile the unit can have leave before waiting.
+  if (tile > 0 && (!scored || row0 >= rows)) return;
   pdl_wait_front();  // q, lengths, KV pages, summaries and selection state are now final
   // The attention reads a non-streaming unit's selection once its count is >= 0: mark
   // it not ready before any attention CTA can start (the buffer's last readers, the
@@ -78,17 +86,23 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   }
   __syncthreads();
   pdl_trigger_front();  // the attention may start launching
+  // Start this tile's summary copy before reading the length (every path below waits
+  // for it in score_tile_finish before returning).
+  const bool spec = scored && off >= 0 && off % 4 == 0;
+  const int n_loaded = score_tile_issue<D, G>(io.summaries + (spec ? off : 0), spec ? row0 : -1, rows, smem, &bar);
+  const Geom none{};
 
   const int T = kv.seq_lens[b];
   const size_t srow = static_cast<size_t>(u) * MS;
   int code = BS_OK;
-  if (!unit_cfg_ok(cls, g, s, k, k_e, sink, local) || T < 1) code = BS_ERR_INVALID_ARG;
+  if (!cfg_ok || T < 1) code = BS_ERR_INVALID_ARG;
   else if (cls == BS_DUAL && (io.evict_logits == nullptr || io.alive == nullptr)) code = BS_ERR_INVALID_ARG;
   else if ((T + g - 1) / g > MB || (T + s - 1) / s > rows || off < 0 ||
            (T + kPage - 1) / kPage > dims.max_pages_per_unit)
     code = BS_ERR_CAPACITY;
   else if (off % 4 != 0) code = BS_ERR_ALIGN;
   if (code != BS_OK) {
+    score_tile_finish<D, G>(n_loaded, false, nullptr, 0, none, 0, reduce, nullptr, smem, &bar, st);
     if (tile == 0) {
       for (int i = tid; i < MS; i += kFrontThreads) io.cur_idx[srow + i] = io.added[srow + i] = io.removed[srow + i] = -1;
       __syncthreads();
@@ -104,17 +118,17 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   const Geom ge = unit_geom(T, g, s, sink, local);
   int n_tiles = 1;
   if (cls != BS_STREAMING) n_tiles = max(1, score_tiles(ge));
-  if (tile >= n_tiles) return;
-
   float *score_row = io.scores + static_cast<size_t>(u) * MB;
-  if (cls != BS_STREAMING && ge.c_hi > ge.c_lo) {
-    const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
-    const void *qrow = dims.q_dtype == BS_BF16
-                           ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
-                           : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
-    if (!score_tile<D, G>(io.summaries + off, qrow, dims.q_dtype, ge, tile, reduce, score_row, smem, &bar, st))
-      return;
-  }
+  // Scored only when the candidates exist, in which case they start at the sink's end
+  // and the rows copied above are this tile's.
+  const bool score = cls != BS_STREAMING && ge.c_hi > ge.c_lo && tile < n_tiles;
+  const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
+  const void *qrow = dims.q_dtype == BS_BF16
+                         ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
+                         : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
+  if (!score_tile_finish<D, G>(n_loaded, score, qrow, dims.q_dtype, ge, tile, reduce, score_row, smem, &bar, st))
+    return;
+  if (tile >= n_tiles) return;
   // ---- a1: the sub-block holding the appended token (tile 0, beside the others) ----
   if (tile == 0 && tid < 32) {
     const int j = (T - 1) / s;
@@ -139,7 +153,6 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   uint8_t *flags = reinterpret_cast<uint8_t *>(keys + MB);
   int32_t *cur_sm = reinterpret_cast<int32_t *>(smem + static_cast<size_t>(MB) * 4 + ((MB + 15) & ~15));
   int32_t *prev_sm = cur_sm + MS;
-  uint32_t *pbits = reinterpret_cast<uint32_t *>(prev_sm + MS);
   // The previous selection is final since the previous step: copy it asynchronously
   // (cp.async) into shared memory; it lands while the selection runs.
   __shared__ int np_sm;
@@ -154,8 +167,7 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   su.scores = score_row;
   su.evict = cls == BS_DUAL ? io.evict_logits + static_cast<size_t>(u) * MB : nullptr;
   su.alive = cls == BS_DUAL ? io.alive + static_cast<size_t>(u) * MB : nullptr;
-  select_unit_flags<kFrontThreads>(su, keys, flags, sh);
-  int total = compact_selection<kFrontThreads>(flags, ge.n_blk, io.cur_idx + srow, MS, cur_sm, sh);
+  int total = select_unit<kFrontThreads>(su, keys, flags, io.cur_idx + srow, MS, cur_sm, sh);
   if (total < 0) {
     if (tid == 0) report(st, BS_ERR_CAPACITY);
     total = 0;
@@ -172,8 +184,7 @@ __global__ void __launch_bounds__(kFrontThreads) step_front_kernel(bs_dims dims,
   }
 
   // ---- a5: set-difference against the previous selection --------------------------
-  const int2 nd = setdiff_after_select<kFrontThreads>(cur_sm, total, prev_sm, np, flags, ge.n_blk, pbits,
-                                                      (MB + 31) / 32, io.added + srow, io.removed + srow, MS, sh);
+  const int2 nd = setdiff_sorted<kFrontThreads>(cur_sm, total, prev_sm, np, io.added + srow, io.removed + srow, MS, sh);
   if (tid == 0) {
     io.added_cnt[u] = nd.x;
     io.removed_cnt[u] = nd.y;
