@@ -85,11 +85,12 @@ size_t bs_workspace_size(const bs_dims *dims) {
   if (bsi::check_dims(dims) != BS_OK) return 0;
   const int G = dims->n_q_heads / dims->n_kv_heads;
   const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
-  // Cluster mode keeps the split partials on chip: only the counters are needed.
-  const size_t records = bsi::attn_cluster_mode(dims->max_gather_pages_per_unit)
-                             ? 0
-                             : units * bsi::kAttnMaxSplits * G * bsi::attn_record_floats(dims->head_dim);
-  return (bsi::attn_counter_floats(units) + records) * sizeof(float);
+  // Cluster mode keeps the split partials on chip: the counters and the fused step's
+  // page lists. Workspace mode: the counters and the split records.
+  const size_t tail = bsi::attn_cluster_mode(dims->max_gather_pages_per_unit)
+                          ? bsi::attn_plist_ints(units, dims->max_gather_pages_per_unit)
+                          : units * bsi::kAttnMaxSplits * G * bsi::attn_record_floats(dims->head_dim);
+  return (bsi::attn_counter_floats(units) + tail) * sizeof(float);
 }
 
 bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *c, const int32_t *seq_lens_host) {

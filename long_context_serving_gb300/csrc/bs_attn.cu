@@ -21,6 +21,7 @@ bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv,
   a.lse = lse;
   a.arrivals = reinterpret_cast<int32_t *>(ws) + units;  // second counter of each unit
   a.records = ws + attn_counter_floats(units);
+  a.plist = nullptr;
   a.st = st;
   return dims->kv_dtype == BS_BF16 ? launch_attn_bf16(a, false, cs) : launch_attn_f32(a, false, cs);
 }

@@ -12,7 +12,7 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnArgs a, const
                                                                bool cluster) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   if (step) pdl_launch_dependents();
-  attn_split_mma<D, G>(a.dims, a.q, a.kv, a.cfg, &tmk, &tmv, a.sel_idx, a.sel_cnt, a.arrivals, a.records, a.out,
+  attn_split_mma<D, G>(a.dims, a.q, a.kv, a.cfg, &tmk, &tmv, a.sel_idx, a.sel_cnt, a.plist, a.arrivals, a.records, a.out,
                        a.lse, a.st, align_smem_1024(smem_raw), step, cluster);
   // In the fused step, finish only after the selection kernel has.
   if (step) pdl_wait();

@@ -10,7 +10,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kFfmaThreads) attn_ffma_kernel(AttnArgs a, bool step, bool cluster) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (step) pdl_launch_dependents();
-  attn_split_ffma<D, G>(a.dims, a.q, a.kv, a.cfg, a.sel_idx, a.sel_cnt, a.arrivals, a.records, a.out, a.lse, a.st,
+  attn_split_ffma<D, G>(a.dims, a.q, a.kv, a.cfg, a.sel_idx, a.sel_cnt, a.plist, a.arrivals, a.records, a.out, a.lse, a.st,
                         smem, step, cluster);
   if (step) pdl_wait();
 }

@@ -77,6 +77,7 @@ struct UnitBlocks {
   int n_sink, lo2;        // computed list: [0, n_sink) then [lo2, lo2 + cnt - n_sink)
   const int32_t *sel;     // selection row (global), when not computed
   const int32_t *sel_sm;  // its first kSelPreload entries in shared memory
+  const int32_t *plist;   // the unit's page list (fused step), or null
   UnitPages pg;
 
   __device__ __forceinline__ int block(int i) const {
@@ -89,8 +90,8 @@ struct UnitBlocks {
 // the unit is streaming) and its split plan. All NT threads call it.
 template <int NT>
 __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
-                                       const int32_t *sel_idx, const int32_t *sel_cnt, int u, int32_t *sel_sm,
-                                       int32_t *st, bool in_step, bool in_cluster) {
+                                       const int32_t *sel_idx, const int32_t *sel_cnt, const int32_t *plist, int u,
+                                       int32_t *sel_sm, int32_t *st, bool in_step, bool in_cluster) {
   __shared__ int sh_cnt;
   const int tid = threadIdx.x, split = blockIdx.x;
   const int b = u / dims.n_kv_heads;
@@ -100,6 +101,7 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
   ub.computed = false;
   ub.sel = sel_idx + static_cast<size_t>(u) * dims.max_sel_per_unit;
   ub.sel_sm = sel_sm;
+  ub.plist = nullptr;
   ub.n_sink = ub.lo2 = 0;
   ub.cnt = 0;
   const bool cfg_ok = ub.g > 0 && ub.g % kPage == 0 && ub.T >= 1;
@@ -110,49 +112,61 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
     ub.lo2 = ge.local_lo > ge.n_sink ? ge.local_lo : ge.n_sink;
     ub.cnt = ge.n_sink + (ge.n_blk - ub.lo2);
   }
-  if (!ub.computed) {
+  if (!ub.computed && !in_step) {
+    // The count and the first entries of the row are read together (entries past the
+    // count are never used).
+    const int ns = min(dims.max_sel_per_unit, kSelPreload);
+    if (tid == 0) sh_cnt = sel_cnt[u];
+    for (int i = tid; i < ns; i += NT) sel_sm[i] = ub.sel[i];
+    __syncthreads();
+    ub.cnt = sh_cnt;
+  } else if (!ub.computed) {
     if (tid == 0) {
-      int c = 0;
-      if (in_step) {
-        // The selection kernel publishes this unit's count with a release store once
-        // the row is written (-1 until then). Poll with relaxed loads and a short sleep
-        // (acquire loads in a tight loop slow down the other CTAs of the SM), then one
-        // acquire fence. Bounded wait: about one second.
-        c = load_relaxed_gpu(sel_cnt + u);
-        if (c < 0) {
-          const uint64_t t0 = global_ns();
-          while ((c = load_relaxed_gpu(sel_cnt + u)) < 0) {
-            __nanosleep(64);
-            if (global_ns() - t0 > 1000000000ull) {
-              report(st, BS_ERR_TIMEOUT);
-              c = 0;
-              break;
-            }
+      // The selection kernel publishes this unit's count with a release store once the
+      // row is written (-1 until then): poll with relaxed loads and a short sleep, then
+      // one acquire fence. Bounded wait: about one second.
+      int c = load_relaxed_gpu(sel_cnt + u);
+      if (c < 0) {
+        const uint64_t t0 = global_ns();
+        while ((c = load_relaxed_gpu(sel_cnt + u)) < 0) {
+          __nanosleep(64);
+          if (global_ns() - t0 > 1000000000ull) {
+            report(st, BS_ERR_TIMEOUT);
+            c = 0;
+            break;
           }
         }
-        fence_acq_rel_gpu();
-      } else {
-        c = sel_cnt[u];
       }
+      fence_acq_rel_gpu();
       sh_cnt = c;
     }
     __syncthreads();
     ub.cnt = sh_cnt;
-    const int ns = min(min(dims.max_sel_per_unit, kSelPreload), max(ub.cnt, 0));
-    for (int i = tid; i < ns; i += NT) sel_sm[i] = in_step ? __ldcg(ub.sel + i) : ub.sel[i];
-    __syncthreads();
+    if (plist != nullptr) {
+      // The selection kernel also wrote the pages of the selected blocks; the last
+      // selected block is the tail block, which is always forced.
+      ub.plist = plist + static_cast<size_t>(u) * dims.max_gather_pages_per_unit;
+    } else {
+      const int ns = min(min(dims.max_sel_per_unit, kSelPreload), max(ub.cnt, 0));
+      for (int i = tid; i < ns; i += NT) sel_sm[i] = __ldcg(ub.sel + i);
+      __syncthreads();
+    }
   }
   ub.ok = cfg_ok && ub.cnt >= 0 && ub.cnt <= dims.max_sel_per_unit;
   if (!ub.ok && split == 0 && tid == 0) report(st, BS_ERR_INVALID_ARG);
   int last = -1;
   if (ub.ok && ub.cnt > 0) {
-    last = ub.block(ub.cnt - 1);
+    last = ub.plist ? (ub.T - 1) / ub.g : ub.block(ub.cnt - 1);
     if (last < 0 || static_cast<int64_t>(last) * ub.g >= ub.T) {
       if (split == 0 && tid == 0) report(st, BS_ERR_DEVICE_BOUNDS);
       ub.ok = false;
     }
   }
   ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster);
+  if (ub.plist && ub.pg.n_pages > dims.max_gather_pages_per_unit) {
+    if (split == 0 && tid == 0) report(st, BS_ERR_CAPACITY);
+    ub.pg.n_pages = 0;
+  }
   return ub;
 }
 
@@ -173,6 +187,16 @@ __device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims 
                                             int gp1, int *phys_out, int32_t *st) {
   *phys_out = -1;
   if (gp >= gp1) return 0;
+  if (ub.plist) {
+    // Pages come resolved; all are full but the unit's last, which holds token T-1.
+    const int phys = __ldcg(ub.plist + gp);
+    if (phys < 0 || phys >= dims.n_pages) {
+      report(st, BS_ERR_DEVICE_BOUNDS);
+      return 0;
+    }
+    *phys_out = phys;
+    return gp == ub.pg.n_pages - 1 ? (ub.T - 1) % kPage + 1 : kPage;
+  }
   const int ppb = ub.pg.ppb;
   const int i = gp / ppb, pb = gp - i * ppb;
   const int c = ub.block(i);
@@ -426,7 +450,8 @@ template <int D, int G>
 __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
                                const bs_head_cfg &cfg, const CUtensorMap *tmk, const CUtensorMap *tmv,
                                const int32_t *__restrict__ sel_idx, const int32_t *__restrict__ sel_cnt,
-                               int32_t *__restrict__ arrivals, float *__restrict__ ws, float *__restrict__ out,
+                               const int32_t *plist, int32_t *__restrict__ arrivals, float *__restrict__ ws,
+                               float *__restrict__ out,
                                float *__restrict__ lse, int32_t *st, unsigned char *smem, bool in_step,
                                bool in_cluster) {
   using L = MmaLayout<D>;
@@ -443,7 +468,7 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st, in_step, in_cluster);
+  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);
     return;
@@ -462,11 +487,21 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   }
   __syncthreads();
 
-  // Warp 0: resolve the 4 pages of a stage and start their copies (one TMA box per
-  // 64-column half of a page, for K and for V).
+  // Warp 0 resolves the split's pages 32 at a time (lane l: page 32 c + l of the split;
+  // one round of page-table loads per chunk) and starts the copies of a stage's 4
+  // pages (one TMA box per 64-column half of a page, for K and for V).
+  int chunk = -1, ch_phys = -1, ch_valid = 0;
   auto issue = [&](int stage, int buf) {
-    int phys = -1, valid_tok = 0;
-    if (lane < kStagePages) valid_tok = resolve_page(ub, dims, pt, gp0 + stage * kStagePages + lane, gp1, &phys, st);
+    const int first = stage * kStagePages;  // stages never straddle a chunk
+    if (first / 32 != chunk) {
+      chunk = first / 32;
+      ch_valid = resolve_page(ub, dims, pt, gp0 + chunk * 32 + lane, gp1, &ch_phys, st);
+    }
+    const int src = first - chunk * 32 + (lane & (kStagePages - 1));
+    const int phys_l = __shfl_sync(0xffffffffu, ch_phys, src);
+    const int valid_l = __shfl_sync(0xffffffffu, ch_valid, src);
+    const int phys = lane < kStagePages ? phys_l : -1;
+    const int valid_tok = lane < kStagePages ? valid_l : 0;
     const unsigned m = __ballot_sync(0xffffffffu, valid_tok > 0);
     if (lane == 0) mbar_arrive_expect_tx(&bars[buf], static_cast<uint32_t>(__popc(m)) * 2u * L::kPageBytes);
     __syncwarp();
@@ -694,7 +729,8 @@ struct FfmaLayout {
 template <int D, int G>
 __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
                                 const bs_head_cfg &cfg, const int32_t *__restrict__ sel_idx,
-                                const int32_t *__restrict__ sel_cnt, int32_t *__restrict__ arrivals,
+                                const int32_t *__restrict__ sel_cnt, const int32_t *plist,
+                                int32_t *__restrict__ arrivals,
                                 float *__restrict__ ws, float *__restrict__ out, float *__restrict__ lse,
                                 int32_t *st, unsigned char *smem, bool in_step, bool in_cluster) {
   using L = FfmaLayout<D, G>;
@@ -711,7 +747,7 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, u, sel_sm, st, in_step, in_cluster);
+  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);
     return;

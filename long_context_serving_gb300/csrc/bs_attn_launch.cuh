@@ -17,6 +17,7 @@ struct AttnArgs {
   float *lse;
   int32_t *arrivals;  // per-unit counters (workspace mode)
   float *records;     // split records (workspace mode)
+  const int32_t *plist;  // fused step, cluster mode: page lists of non-streaming units, else null
   int32_t *st;
 };
 

@@ -17,7 +17,13 @@ __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 
 // The workspace starts with two int32 arrival counters per unit (the selection phase
 // of the fused decode step, then the attention in workspace mode), padded to 16 bytes.
+// After them: in cluster mode the fused step's page lists (int32 [units][max gather
+// pages]: the physical pages of each unit's selected blocks in attention order), in
+// workspace mode the split records.
 __host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (2 * units + 3) / 4 * 4; }
+__host__ __device__ constexpr size_t attn_plist_ints(size_t units, int max_gather) {
+  return (units * static_cast<size_t>(max_gather) + 3) / 4 * 4;
+}
 
 // Cluster mode: a unit's splits are the 16 CTAs of one cluster and merge through
 // distributed shared memory. Workspace mode (selections above 1024 pages): up to 32

@@ -28,7 +28,7 @@ constexpr int kBuckets = 2048;  // histogram buckets of the fast top-k
 constexpr int kBndDirect = 256; // boundary buckets up to this size are ranked directly
 
 template <int NT>
-struct SelShared {
+struct __align__(16) SelShared {  // hist is cleared with 16-byte stores
   static constexpr int kWarps = NT / 32;
   uint32_t hist[kBuckets];      // the radix passes use the first 256
   int warp_tot[kWarps];
@@ -51,6 +51,8 @@ __device__ __forceinline__ bool sorted_contains(const int32_t *v, int n, int x) 
   }
   return lo < n && v[lo] == x;
 }
+
+static_assert(alignof(SelShared<256>) >= 16 && alignof(SelShared<512>) >= 16, "16-byte stores into hist");
 
 // Exclusive prefix sum of one int per thread over the CTA; *total gets the sum.
 template <int NT>
@@ -423,12 +425,9 @@ template <int NT>
 __device__ __forceinline__ void block_min_max_count(uint32_t &kmin, uint32_t &kmax, int &cnt, SelShared<NT> &sh) {
   constexpr int W = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  cnt = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(cnt)));
   if (lane == 0) {
     sh.warp_min[warp] = kmin;
     sh.warp_max[warp] = kmax;
@@ -496,7 +495,7 @@ __device__ __forceinline__ uint32_t topk_regs(const uint32_t (&key)[R], uint32_t
         kmax = max(kmax, key[i]);
         ++cnt;
       }
-    for (int j = tid; j < kBuckets; j += NT) sh.hist[j] = 0u;
+    for (int j = tid; j < kBuckets / 4; j += NT) reinterpret_cast<uint4 *>(sh.hist)[j] = make_uint4(0u, 0u, 0u, 0u);
     block_min_max_count<NT>(kmin, kmax, cnt, sh);
     if (need >= cnt) {
       take |= E;
@@ -515,14 +514,23 @@ __device__ __forceinline__ uint32_t topk_regs(const uint32_t (&key)[R], uint32_t
     const int shift = bits > 11 ? bits - 11 : 0;
     auto bucket = [&](uint32_t kk) -> uint32_t {
       if (bscale > 0.0f) {
-        const float f = (key_value(kk) - xmin) * bscale;  // in [0, 2048 (1 + eps)]
-        return f >= static_cast<float>(kBuckets - 1) ? static_cast<uint32_t>(kBuckets - 1) : static_cast<uint32_t>(f);
+        // f in [0, 2048 (1 + eps)]; adding 2^23 rounds it to an integer in the low
+        // mantissa bits (monotone, like every step here).
+        const float f = (key_value(kk) - xmin) * bscale;
+        const uint32_t rb = __float_as_uint(f + 8388608.0f) - 0x4B000000u;
+        return min(rb, static_cast<uint32_t>(kBuckets - 1));
       }
       return (kk - kmin) >> shift;
     };
+    constexpr bool kCache = R <= 8;  // bucket of each element kept in registers
+    uint32_t bkc[kCache ? R : 1];
 #pragma unroll
     for (int i = 0; i < R; ++i)
-      if (i < nr && ((E >> i) & 1u)) atomicAdd(&sh.hist[bucket(key[i])], 1u);
+      if (i < nr && ((E >> i) & 1u)) {
+        const uint32_t bk = bucket(key[i]);
+        if (kCache) bkc[kCache ? i : 0] = bk;
+        atomicAdd(&sh.hist[bk], 1u);
+      }
     __syncthreads();
     // Thread t owns buckets [kBuckets - bpt (t + 1), kBuckets - bpt t), highest first.
     const int top = kBuckets - bpt * tid - 1;
@@ -555,7 +563,7 @@ __device__ __forceinline__ uint32_t topk_regs(const uint32_t (&key)[R], uint32_t
 #pragma unroll
     for (int i = 0; i < R; ++i)
       if (i < nr && ((E >> i) & 1u)) {
-        const uint32_t bk = bucket(key[i]);
+        const uint32_t bk = kCache ? bkc[kCache ? i : 0] : bucket(key[i]);
         if (bk > B) take |= 1u << i;
         else if (bk == B) nextE |= 1u << i;
       }

@@ -40,21 +40,25 @@ __device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
 
 // Shared memory of the selection phase: keys [MB] u32 and flags [MB] u8 (padded to
 // 16; used by selections above 32 candidates per thread), current and previous
-// selection [MS] i32 each.
+// selection [MS] i32 each, then (page lists in cluster mode, tables up to 64 KB) the
+// unit's page-table row [max_pages] i32.
+constexpr int kPtCacheInts = 16384;
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel) {
+__host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel, int pt_cache_ints) {
   const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
-  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4;
+  return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4 +
+         static_cast<size_t>(pt_cache_ints) * 4;
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
-                                                                   bs_step_io io, int reduce, int32_t *arrivals) {
+                                                                   bs_step_io io, int reduce, int32_t *arrivals,
+                                                                   int32_t *plist, int pt_cache_ints) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t bar;
   __shared__ SelShared<kFrontThreads> sh;
@@ -153,11 +157,19 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   uint8_t *flags = reinterpret_cast<uint8_t *>(keys + MB);
   int32_t *cur_sm = reinterpret_cast<int32_t *>(smem + static_cast<size_t>(MB) * 4 + ((MB + 15) & ~15));
   int32_t *prev_sm = cur_sm + MS;
+  int32_t *pt_sm = prev_sm + MS;
   // The previous selection is final since the previous step: copy it asynchronously
-  // (cp.async) into shared memory; it lands while the selection runs.
+  // (cp.async) into shared memory; it lands while the selection runs. So does the
+  // unit's page-table row when the page list is written from shared memory.
   __shared__ int np_sm;
   if (tid == 0) cp_async4(&np_sm, io.prev_cnt + u);
   for (int i = tid; i < MS; i += kFrontThreads) cp_async4(prev_sm + i, io.prev_idx + srow + i);
+  const bool mk_plist = plist != nullptr && cls != BS_STREAMING;
+  const int32_t *pt_row = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+  const int n_lp = min(dims.max_pages_per_unit, (T + kPage - 1) / kPage);
+  const bool pt_cached = mk_plist && pt_cache_ints >= n_lp;
+  if (pt_cached)
+    for (int i = tid; i < n_lp; i += kFrontThreads) cp_async4(pt_sm + i, pt_row + i);
   cp_async_commit();
   SelUnit su;
   su.cls = cls;
@@ -172,7 +184,31 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
     if (tid == 0) report(st, BS_ERR_CAPACITY);
     total = 0;
   }
-  // Publish: the row is written; the count (release) tells the attention it is ready.
+  if (mk_plist) {
+    // Page list for the attention: the pages of the selected blocks in order (the
+    // last selected block is the tail block; its pages past T are left out), -1 for
+    // an entry outside the table or the pool.
+    cp_async_wait_all();
+    __syncthreads();
+    const int ppb = g / kPage;
+    const int tail_pages = min(ppb, (T - (ge.n_blk - 1) * g + kPage - 1) / kPage);
+    const int n_pages = total > 0 ? (total - 1) * ppb + tail_pages : 0;
+    int32_t *pl = plist + static_cast<size_t>(u) * dims.max_gather_pages_per_unit;
+    if (n_pages <= dims.max_gather_pages_per_unit)
+      for (int i = tid; i < n_pages; i += kFrontThreads) {
+        const int blk = i / ppb, pb = i - blk * ppb;
+        const int c = cur_sm[blk];
+        const int lp = c * ppb + pb;
+        int phys = -1;
+        if (c >= 0 && lp < n_lp && c * g + pb * kPage < T) {
+          phys = pt_cached ? pt_sm[lp] : __ldg(pt_row + lp);
+          if (phys < 0 || phys >= dims.n_pages) phys = -1;
+        }
+        pl[i] = phys;
+      }
+  }
+  // Publish: the row and the page list are written; the count (release) tells the
+  // attention they are ready.
   __syncthreads();
   if (tid == 0) store_release(io.cur_cnt + u, total);
   cp_async_wait_all();
@@ -201,13 +237,20 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
   if (!attr_ok) return BS_ERR_CUDA;
   const int units = dims.batch * dims.n_kv_heads;
-  size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit);
+  const bool cluster = attn_cluster_mode(dims.max_gather_pages_per_unit);
+  int pt_cache = cluster && dims.max_pages_per_unit <= kPtCacheInts ? dims.max_pages_per_unit : 0;
+  size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, pt_cache);
+  if (front_smem > kFrontMaxSmem) {  // read the page table from global memory instead
+    pt_cache = 0;
+    front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, 0);
+  }
   if (front_smem < static_cast<size_t>(ScoreLayout<D, G>::kBytes)) front_smem = ScoreLayout<D, G>::kBytes;
   if (front_smem > kFrontMaxSmem) return BS_ERR_CAPACITY;
   int32_t *counters = static_cast<int32_t *>(io.workspace);
+  int32_t *plist = cluster ? counters + attn_counter_floats(units) : nullptr;
   const dim3 front_grid(units, dims.max_subs_per_unit / kTileRows + 2);
   if (launch_ex(step_front_kernel<D, G>, front_grid, kFrontThreads, front_smem, cs, 0, true, dims, kv, cfg, io,
-                reduce, counters) != cudaSuccess)
+                reduce, counters, plist, pt_cache) != cudaSuccess)
     return BS_ERR_CUDA;
   AttnArgs a;
   a.dims = dims;
@@ -220,6 +263,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
   a.lse = io.lse;
   a.arrivals = counters + units;
   a.records = static_cast<float *>(io.workspace) + attn_counter_floats(units);
+  a.plist = plist;
   a.st = io.dev_status;
   return dims.kv_dtype == BS_BF16 ? launch_attn_bf16(a, true, cs) : launch_attn_f32(a, true, cs);
 }
