@@ -39,14 +39,24 @@ CFG_ID = 2
 LAYERS = 32
 WORKLOAD = ("llama3.1-8b decode layer: B=1, Hq=32, Hkv=8, d=128, T=32768, g=32, s=8; "
             "4 streaming heads (sink 128 + window 2048), 4 retrieval heads (5% budget = 51 blocks)")
+# Other workloads of the same path (--config), measured beside the headline one; layer
+# counts keep each step's working set several times the L2 within a few GB of HBM.
+WORKLOADS = {
+    2: (WORKLOAD, 32),
+    3: ("llama3.1-8b decode layer at 128K, mixed heads: B=4, Hq=32, Hkv=8, d=128, T=131069, per-unit "
+        "g in {16,32,64,128} (s=g/4), budget 2-10%, streaming/retrieval 50/50", 4),
+    4: ("qwen2.5-7b decode layer, low-rank K/V: B=8, Hq=28, Hkv=4, d=128, T_b in [32768, 65536], g=64, "
+        "s=16, all retrieval, 5% budget", 8),
+    5: ("nosa dual selection: B=64, Hq=32, Hkv=8, d=128, T=16377, g=64, s=16, k=32, k_e=24", 2),
+}
 FALLBACK_HBM_GBS = 6800.0
 PAGE = 16
 
 
 def _config(extra=None):
     c = {"workload": WORKLOAD, "layers_per_step": LAYERS, "kv_dtype": "bf16", "q_dtype": "bf16",
-         "l2": "inputs larger than L2: 32 distinct layer buffers, ~0.5 GB touched per step",
-         "graph": "CUDA graph of 32 layers x 5 calls"}
+         "l2": f"inputs larger than L2: {LAYERS} distinct layer buffers per step",
+         "graph": f"CUDA graph of {LAYERS} layers"}
     if extra:
         c.update(extra)
     return c
@@ -162,17 +172,19 @@ def _geom(T, g, sink, local):
 
 def algorithmic_bytes(wl, sel_lists, prev_lists):
     d, G = wl.d, wl.G
-    T = wl.T(0, 0)
     out = {"score": 0, "attn": 0, "select": 0, "setdiff": 0, "summary_update": 0}
     for u in range(wl.U):
+        T = wl.T(0, u // wl.Hkv)
         g, s = int(wl.g[u]), int(wl.s[u])
         n_blk, _, _, c_lo, c_hi = _geom(T, g, int(wl.sink[u]), int(wl.local[u]))
         n_cand = c_hi - c_lo
         # a1: the touched sub-block's tokens read, one summary row written
         out["summary_update"] += (((T - 1) % s) + 1) * d * 2 + d * 4
         if wl.cls[u] != 0:
-            out["score"] += n_cand * (g // s) * d * 4 + G * d * 2 + n_cand * 4
-            out["select"] += n_cand * 4 + len(sel_lists[u]) * 4
+            # dual units need no scores of their Gamma_e blocks
+            n_scored = n_cand - (min(int(wl.k_e[u]), n_cand) if wl.cls[u] == 2 else 0)
+            out["score"] += n_scored * (g // s) * d * 4 + G * d * 2 + n_scored * 4
+            out["select"] += n_cand * 4 + len(sel_lists[u]) * 4 + (n_blk * 5 if wl.cls[u] == 2 else 0)
         sel = sel_lists[u]
         tokens = sum(min(g, T - c * g) for c in sel)
         pages = sum(-(-min(g, T - c * g) // PAGE) for c in sel)
@@ -361,7 +373,7 @@ def run_ours(args) -> None:
     achieved = nbytes[dominant] / (per_kernel[dominant] * 1e-6) / 1e9
     attn_kernel = "attn_mma_kernel" if wl.dtype == "bf16" else "attn_ffma_kernel"
     kernel_name = {"attn": attn_kernel, "score": "score_kernel"}[dominant]
-    traffic = _measured_traffic(kernel_name, "llama8b-32k")
+    traffic = _measured_traffic(kernel_name, wl.name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel_name,
                 "peak_source": peak_note, "algorithmic_bytes_per_launch": nbytes[dominant],
@@ -432,10 +444,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "calls"], default="fused",
                     help="fused: bs_decode_step per layer; calls: the five separate calls per layer")
-    ap.add_argument("--layers", type=int, default=LAYERS,
+    ap.add_argument("--layers", type=int, default=None,
                     help="layer buffers per step (fewer only for profiling small cases)")
+    ap.add_argument("--config", type=int, choices=sorted(WORKLOADS), default=CFG_ID,
+                    help="workload (2, the default, is the headline one)")
     args = ap.parse_args()
-    globals()["LAYERS"] = args.layers
+    globals()["CFG_ID"] = args.config
+    globals()["WORKLOAD"], default_layers = WORKLOADS[args.config]
+    globals()["LAYERS"] = args.layers if args.layers else default_layers
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

@@ -106,15 +106,21 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for a barrier phase with a wall-clock limit (about one second). Returns false
-// and records BS_ERR_TIMEOUT if the phase never completes.
+// Wait for a barrier phase with a wall-clock limit (about one second; the timer is
+// read every 64 tries only). Returns false and records BS_ERR_TIMEOUT if the phase
+// never completes.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *st) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  uint32_t n = 0;
+  uint64_t t0 = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > 1000000000ull) {
-      report(st, BS_ERR_TIMEOUT);
-      return false;
+    if ((++n & 63u) == 0) {
+      const uint64_t t = global_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > 1000000000ull) {
+        report(st, BS_ERR_TIMEOUT);
+        return false;
+      }
     }
   }
   return true;

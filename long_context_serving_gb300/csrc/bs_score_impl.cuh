@@ -5,10 +5,11 @@
 // Fluxion", Systeemcomponenten, "Granularity-Budget Selector").
 //
 // One CTA of 256 threads scores a tile of 64 consecutive summary rows (64/r whole
-// blocks, r = g/s). The tile arrives in shared memory with one bulk copy; four threads
-// share a row, each taking every fourth 16-byte chunk in a row-rotated order so that
-// the 8 lanes of a shared-memory phase hit 8 different bank groups. The G query vectors
-// (pre-scaled by 1/sqrt(d)) sit in shared memory and are read as broadcasts.
+// blocks, r = g/s). The tile arrives in shared memory with one bulk copy. Each warp
+// takes 8 rows; each lane keeps its slice of the G query vectors (pre-scaled by
+// 1/sqrt(d)) in registers and reads its slice of every row once, and a butterfly
+// reduce-scatter across the lanes completes the dot products: shared memory is read
+// once per summary byte.
 #pragma once
 
 #include <math.h>
@@ -82,37 +83,75 @@ __device__ bool score_tile_finish(int n_loaded, bool score, const void *qrow, in
   const int nb = min(bpt, ge.c_hi - c_first);
   const int nrows = min(nb * r, n_loaded);
 
-  // Dot products: thread (row, quarter).
-  constexpr int kChunks = D / 4;     // float4 chunks per row
-  constexpr int kPer = kChunks / 4;  // chunks per quarter (power of two)
-  const int row = tid >> 2, qq = tid & 3;
-  float acc[G];
+  // Dot products. Warp w takes rows 8w .. 8w+7 of the tile; lane l owns dimensions
+  // [l*DPL, (l+1)*DPL) and keeps the G query slices of them in registers, so shared
+  // memory is read once per row (a contiguous row per warp). Each lane forms the
+  // 8 x G partial sums of its dimensions; a butterfly reduce-scatter over the 32
+  // lanes (values halved at each of 5 stages) leaves lane l with the full sums of
+  // entries [l*NF, (l+1)*NF) of the row-major (row, head) list.
+  static_assert(D % 32 == 0 && D / 32 <= 4, "head_dim 32..128");
+  constexpr int DPL = D / 32;
+  constexpr int GP = G <= 4 ? 4 : 8;  // heads padded to a power of two
+  constexpr int PV = 8 * GP;          // partials per lane: 32 or 64
+  constexpr int NF = PV / 32;         // full sums per lane after the reduction
+  const int lane = tid & 31, warp = tid >> 5;
+  float qv[G][DPL];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-  if (row < nrows) {
-    const float4 *rp = reinterpret_cast<const float4 *>(tile_sm + row * D);
+  for (int h = 0; h < G; ++h)
 #pragma unroll
-    for (int c = 0; c < kPer; ++c) {
-      const int ch = qq + 4 * ((c + row) & (kPer - 1));
-      const float4 k4 = rp[ch];
+    for (int j = 0; j < DPL; ++j) qv[h][j] = qs[h * D + lane * DPL + j];
+  float part[PV];
+#pragma unroll
+  for (int i = 0; i < PV; ++i) part[i] = 0.0f;
+#pragma unroll
+  for (int rr = 0; rr < 8; ++rr) {
+    const int row = warp * 8 + rr;
+    if (row < nrows) {
+      float kv[DPL];
+      const float *rp = tile_sm + row * D + lane * DPL;
+      if constexpr (DPL == 4) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(rp);
+        kv[0] = k4.x;
+        kv[1] = k4.y;
+        kv[2] = k4.z;
+        kv[3] = k4.w;
+      } else if constexpr (DPL == 2) {
+        const float2 k2 = *reinterpret_cast<const float2 *>(rp);
+        kv[0] = k2.x;
+        kv[1] = k2.y;
+      } else {
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) kv[j] = rp[j];
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float4 q4 = reinterpret_cast<const float4 *>(qs + h * D)[ch];
-        acc[h] = fmaf(q4.x, k4.x, acc[h]);
-        acc[h] = fmaf(q4.y, k4.y, acc[h]);
-        acc[h] = fmaf(q4.z, k4.z, acc[h]);
-        acc[h] = fmaf(q4.w, k4.w, acc[h]);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) acc = fmaf(qv[h][j], kv[j], acc);
+        part[rr * GP + h] = acc;
+      }
+    }
+  }
+  // Reduce-scatter: at offset o the lane keeps the half of its values selected by
+  // (lane & o) and adds the partner's copy of that half.
+#pragma unroll
+  for (int o = 16, n = PV; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < PV / 2; ++i) {
+      if (i < n / 2) {
+        const float send = upper ? part[i] : part[i + n / 2];
+        const float keep = upper ? part[i + n / 2] : part[i];
+        part[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
   }
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
-    acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 2);
-  }
-  if (row < nrows && qq == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) dots[row * G + h] = acc[h];
+  for (int j = 0; j < NF; ++j) {
+    const int idx = lane * NF + j;
+    const int rr = idx / GP, h = idx % GP;
+    const int row = warp * 8 + rr;
+    if (h < G && row < nrows) dots[row * G + h] = part[j];
   }
   __syncthreads();
   // Max over the r sub-blocks of a block per head, then over (or mean across) heads.
