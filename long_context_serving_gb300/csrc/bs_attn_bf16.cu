@@ -28,9 +28,10 @@ bs_status launch_modes(const AttnArgs &a, bool step, const CUtensorMap &tk, cons
   if (!attrs_ok) return BS_ERR_CUDA;
   const bool cluster = attn_cluster_mode(a.dims.max_gather_pages_per_unit);
   const int units = a.dims.batch * a.dims.n_kv_heads;
-  const dim3 grid(attn_grid_splits(a.dims.max_gather_pages_per_unit), units);
+  const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
+  const dim3 grid(splits, units);
   const cudaError_t e =
-      launch_ex(kernel, grid, kMmaThreads, kSmem, cs, cluster ? kClusterSplits : 0, step, a, tk, tv, step, cluster);
+      launch_ex(kernel, grid, kMmaThreads, kSmem, cs, cluster && splits > 1 ? splits : 0, step, a, tk, tv, step, cluster);
   return e == cudaSuccess ? BS_OK : BS_ERR_CUDA;
 }
 

@@ -162,7 +162,7 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
       ub.ok = false;
     }
   }
-  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster);
+  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster ? static_cast<int>(gridDim.x) : 0);
   if (ub.plist && ub.pg.n_pages > dims.max_gather_pages_per_unit) {
     if (split == 0 && tid == 0) report(st, BS_ERR_CAPACITY);
     ub.pg.n_pages = 0;
@@ -340,15 +340,16 @@ __device__ __forceinline__ float4 ld_peer4(uint32_t a) {
   return v;
 }
 
-// Every CTA of the cluster holds its split's unnormalised o [G][D], m [G] (log2
-// units) and l [G] in shared memory (an idle split: m = -inf, l = 0, o = 0). After a
-// cluster barrier CTA r merges float4 columns r, r + 16, ... of the output over the 16
-// splits in split order; a second barrier keeps every CTA alive until its peers have
-// read it. All threads of all CTAs of the cluster call it.
-template <int NT, int D, int G>
-__device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm, const float *l_sm, float *out,
-                              float *lse) {
-  constexpr int C = kClusterSplits, QD = D / 4, NF4 = G * QD;
+// Every CTA of the cluster (C splits of one unit) holds its split's unnormalised
+// o [G][D], m [G] (log2 units) and l [G] in shared memory (an idle split: m = -inf,
+// l = 0, o = 0). After a cluster barrier CTA r merges float4 columns r, r + C, ... of
+// the output over the C splits in split order (all peer loads of a column issued
+// before their use); a second barrier keeps every CTA alive until its peers have read
+// it. All threads of all CTAs of the cluster call it.
+template <int NT, int D, int G, int C>
+__device__ void cluster_merge_c(size_t orow0, const float *o_sm, const float *m_sm, const float *l_sm, float *out,
+                                float *lse) {
+  constexpr int QD = D / 4, NF4 = G * QD;
   cluster_sync_all();
   const uint32_t rank = cluster_rank();
   for (int i = static_cast<int>(rank) + C * static_cast<int>(threadIdx.x); i < NF4; i += C * NT) {
@@ -361,17 +362,19 @@ __device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm
       lp[p] = ld_peer(peer_addr(l_sm + h, p));
       M = fmaxf(M, mp[p]);
     }
+    float4 v[C];
+#pragma unroll
+    for (int p = 0; p < C; ++p) v[p] = ld_peer4(peer_addr(o_sm + h * D + dq * 4, p));
     float Lsum = 0.0f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int p = 0; p < C; ++p) {
       const float w = (mp[p] == -INFINITY) ? 0.0f : exp2f(mp[p] - M);
       Lsum = fmaf(lp[p], w, Lsum);
-      const float4 v = ld_peer4(peer_addr(o_sm + h * D + dq * 4, p));
-      o.x = fmaf(v.x, w, o.x);
-      o.y = fmaf(v.y, w, o.y);
-      o.z = fmaf(v.z, w, o.z);
-      o.w = fmaf(v.w, w, o.w);
+      o.x = fmaf(v[p].x, w, o.x);
+      o.y = fmaf(v[p].y, w, o.y);
+      o.z = fmaf(v[p].z, w, o.z);
+      o.w = fmaf(v[p].w, w, o.w);
     }
     const float inv = 1.0f / Lsum;
     o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
@@ -379,6 +382,30 @@ __device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm
     if (dq == 0) lse[orow0 + h] = (M + log2f(Lsum)) * kLn2;
   }
   cluster_sync_all();
+}
+
+// Merge of the C = gridDim.x splits of a cluster (a power of two up to 16); a single
+// split normalises its own state.
+template <int NT, int D, int G>
+__device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm, const float *l_sm, float *out,
+                              float *lse) {
+  constexpr int QD = D / 4, NF4 = G * QD;
+  switch (gridDim.x) {
+    case 2: cluster_merge_c<NT, D, G, 2>(orow0, o_sm, m_sm, l_sm, out, lse); return;
+    case 4: cluster_merge_c<NT, D, G, 4>(orow0, o_sm, m_sm, l_sm, out, lse); return;
+    case 8: cluster_merge_c<NT, D, G, 8>(orow0, o_sm, m_sm, l_sm, out, lse); return;
+    case 16: cluster_merge_c<NT, D, G, 16>(orow0, o_sm, m_sm, l_sm, out, lse); return;
+    default: break;
+  }
+  for (int i = threadIdx.x; i < NF4; i += NT) {
+    const int h = i / QD, dq = i % QD;
+    const float L = l_sm[h];
+    const float inv = 1.0f / L;
+    float4 o = reinterpret_cast<const float4 *>(o_sm + h * D)[dq];
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
+    if (dq == 0) lse[orow0 + h] = (m_sm[h] + log2f(L)) * kLn2;
+  }
 }
 
 // ===========================================================================

@@ -26,6 +26,19 @@ struct AttnArgs {
 bs_status launch_attn_bf16(const AttnArgs &a, bool step, cudaStream_t cs);
 bs_status launch_attn_f32(const AttnArgs &a, bool step, cudaStream_t cs);
 
+// About two CTAs per SM of the current device (the attention's split target).
+inline int attn_target_ctas() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 2 * 148;
+  if (cached[dev] == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
+    cached[dev] = 2 * sms;
+  }
+  return cached[dev];
+}
+
 // cudaLaunchKernelEx with an optional cluster width and programmatic serialization.
 template <typename K, typename... Args>
 cudaError_t launch_ex(K kernel, dim3 grid, int threads, size_t smem, cudaStream_t cs, int cluster_x, bool pdl,

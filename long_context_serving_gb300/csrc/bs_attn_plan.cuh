@@ -7,7 +7,9 @@ namespace bsi {
 
 constexpr int kStagePages = 4;                     // pages staged per pipeline step
 constexpr int kStageTokens = kStagePages * kPage;  // 64 tokens
-constexpr int kClusterSplits = 16;                 // splits of a unit in one thread-block cluster
+constexpr int kClusterSplits = 16;                 // most splits of a unit in one thread-block cluster
+constexpr int kSplitTargetPages = 128;             // cluster mode: at most this many pages per split
+                                                   // unless 16 splits are reached
 constexpr int kClusterMaxPages = 1024;             // largest selection (pages) the cluster mode takes
 constexpr int kAttnMaxSplits = 32;                 // splits of a unit in the workspace mode
 
@@ -32,9 +34,20 @@ __host__ __device__ inline bool attn_cluster_mode(int max_gather_pages) {
   return max_gather_pages <= kClusterMaxPages;
 }
 
+// Splits of a unit in cluster mode: a power of two, the smallest that gives the
+// launch at least `target_ctas` CTAs (about two per SM) and keeps every split at or
+// below kSplitTargetPages pages, at most 16. Many units: few long splits (the fixed
+// per-CTA latency is paid once per many pages); few units: 16 splits.
+__host__ __device__ inline int attn_cluster_splits(int units, int max_gather_pages, int target_ctas) {
+  int s = 1;
+  while (s < kClusterSplits && static_cast<long long>(units) * s < target_ctas) s <<= 1;
+  while (s < kClusterSplits && (max_gather_pages + s - 1) / s > kSplitTargetPages) s <<= 1;
+  return s;
+}
+
 // Splits launched per unit.
-__host__ __device__ inline int attn_grid_splits(int max_gather_pages) {
-  if (attn_cluster_mode(max_gather_pages)) return kClusterSplits;
+__host__ __device__ inline int attn_grid_splits(int units, int max_gather_pages, int target_ctas) {
+  if (attn_cluster_mode(max_gather_pages)) return attn_cluster_splits(units, max_gather_pages, target_ctas);
   int splits = (max_gather_pages + kStagePages - 1) / kStagePages;
   if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
   return splits < 1 ? 1 : splits;
@@ -49,8 +62,9 @@ struct UnitPages {
   int n_split;
 };
 
-// The split plan depends only on the unit's own page count and the mode.
-__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk, bool cluster) {
+// The split plan depends only on the unit's own page count and the launch's splits per
+// unit in cluster mode (cluster_splits; 0 in workspace mode).
+__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk, int cluster_splits) {
   UnitPages p;
   p.ppb = g / kPage;
   p.n_pages = 0;
@@ -60,8 +74,8 @@ __device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_
   const int rem_pages = (T - last_blk * g + kPage - 1) / kPage;
   const int last_pages = rem_pages < p.ppb ? rem_pages : p.ppb;
   p.n_pages = (cnt - 1) * p.ppb + last_pages;
-  if (cluster) {
-    p.pps = (p.n_pages + kClusterSplits - 1) / kClusterSplits;
+  if (cluster_splits > 0) {
+    p.pps = (p.n_pages + cluster_splits - 1) / cluster_splits;
   } else {
     int per = (p.n_pages + kStagePages * kAttnMaxSplits - 1) / (kStagePages * kAttnMaxSplits);
     if (per < 1) per = 1;

@@ -87,6 +87,17 @@ def test_parity_large_selection_workspace_merge(fused):
     rep.check()
 
 
+@pytest.mark.parametrize("B", [10, 40])
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_few_splits_per_unit(B, fused):
+    """Many units: the attention takes 4 (B=10) or 1 (B=40) splits per unit."""
+    wl = make_workload(5, seed=3, B=B, T=3000, steps=2)
+    wl.k[:] = 20
+    wl.k_e[:] = 12
+    rep = run_parity(wl, fused=fused)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
