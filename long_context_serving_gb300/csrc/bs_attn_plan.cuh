@@ -8,8 +8,6 @@ namespace bsi {
 constexpr int kStagePages = 4;                     // pages staged per pipeline step
 constexpr int kStageTokens = kStagePages * kPage;  // 64 tokens
 constexpr int kClusterSplits = 16;                 // most splits of a unit in one thread-block cluster
-constexpr int kSplitTargetPages = 128;             // cluster mode: at most this many pages per split
-                                                   // unless 16 splits are reached
 constexpr int kClusterMaxPages = 1024;             // largest selection (pages) the cluster mode takes
 constexpr int kAttnMaxSplits = 32;                 // splits of a unit in the workspace mode
 
@@ -34,20 +32,20 @@ __host__ __device__ inline bool attn_cluster_mode(int max_gather_pages) {
   return max_gather_pages <= kClusterMaxPages;
 }
 
-// Splits of a unit in cluster mode: a power of two, the smallest that gives the
-// launch at least `target_ctas` CTAs (about two per SM) and keeps every split at or
-// below kSplitTargetPages pages, at most 16. Many units: few long splits (the fixed
-// per-CTA latency is paid once per many pages); few units: 16 splits.
-__host__ __device__ inline int attn_cluster_splits(int units, int max_gather_pages, int target_ctas) {
-  int s = 1;
-  while (s < kClusterSplits && static_cast<long long>(units) * s < target_ctas) s <<= 1;
-  while (s < kClusterSplits && (max_gather_pages + s - 1) / s > kSplitTargetPages) s <<= 1;
+// Splits of a unit in cluster mode: the largest power of two (at most 16) that keeps
+// the launch within one wave of `slots` CTAs (about two per SM), at least 1. Few units:
+// 16 short splits each; many units: one wave of long splits, so the fixed latency of
+// a CTA's start (count, row, page table, first copy) is paid once per many pages.
+__host__ __device__ inline int attn_cluster_splits(int units, int max_gather_pages, int slots) {
+  (void)max_gather_pages;
+  int s = kClusterSplits;
+  while (s > 1 && static_cast<long long>(units) * s > slots) s >>= 1;
   return s;
 }
 
 // Splits launched per unit.
-__host__ __device__ inline int attn_grid_splits(int units, int max_gather_pages, int target_ctas) {
-  if (attn_cluster_mode(max_gather_pages)) return attn_cluster_splits(units, max_gather_pages, target_ctas);
+__host__ __device__ inline int attn_grid_splits(int units, int max_gather_pages, int slots) {
+  if (attn_cluster_mode(max_gather_pages)) return attn_cluster_splits(units, max_gather_pages, slots);
   int splits = (max_gather_pages + kStagePages - 1) / kStagePages;
   if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
   return splits < 1 ? 1 : splits;

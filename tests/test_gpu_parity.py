@@ -90,7 +90,7 @@ def test_parity_large_selection_workspace_merge(fused):
 @pytest.mark.parametrize("B", [10, 40])
 @pytest.mark.parametrize("fused", [False, True])
 def test_parity_few_splits_per_unit(B, fused):
-    """Many units: the attention takes 4 (B=10) or 1 (B=40) splits per unit."""
+    """Many units: the attention takes 2 (B=10, 80 units) or 1 (B=40) splits per unit."""
     wl = make_workload(5, seed=3, B=B, T=3000, steps=2)
     wl.k[:] = 20
     wl.k_e[:] = 12
