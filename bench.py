@@ -230,6 +230,65 @@ def _peak_hbm():
 
 
 # ---------------------------------------------------------------------------
+# Block swap from host memory (the offload path): bandwidth of a full cache refill
+# ---------------------------------------------------------------------------
+def measure_block_swap(layer, wl, B, torch, reps: int = 20) -> dict:
+    """Time bs_block_swap filling an empty GPU block cache with one layer's whole
+    selection from pinned host memory (every selected page, K and V, crosses the host
+    link once per call), alternating with a call that empties it."""
+    dev = layer.device
+    U, MS = wl.U, layer.max_sel
+    slots, pps = MS, int(wl.g.max()) // 16
+    n = U * slots * pps
+    ck = torch.empty((n, 16, wl.d), dtype=layer.k_pool.dtype, device=dev)
+    cv = torch.empty_like(ck)
+    cpt = torch.full_like(layer.page_table, -1)
+    sb = torch.full((U, slots), -1, dtype=torch.int32, device=dev)
+    bsl = torch.full((U, layer.max_blocks), -1, dtype=torch.int32, device=dev)
+    cache = B.BlockCache(k_pool=ck.data_ptr(), v_pool=cv.data_ptr(), page_table=cpt.data_ptr(),
+                         slot_block=sb.data_ptr(), block_slot=bsl.data_ptr(), slots_per_unit=slots, pages_per_slot=pps)
+    hk = layer.k_pool.cpu().pin_memory()
+    hv = layer.v_pool.cpu().pin_memory()
+    host = B.HostKV(k_pool=hk.data_ptr(), v_pool=hv.data_ptr(), page_table=layer.page_table.data_ptr(),
+                    n_pages=int(wl.n_pages))
+    sel, cnt = layer.sel[0], layer.cnt[0]
+    zero = torch.zeros_like(cnt)
+    T = layer.seq_lens[0]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lists = layer.selection(0)
+    Tn = [int(wl.T(0, u // wl.Hkv)) for u in range(U)]
+    pages = sum(-(-min(int(wl.g[u]), Tn[u] - c * int(wl.g[u])) // PAGE) for u in range(U) for c in lists[u])
+    nbytes = pages * 2 * PAGE * wl.d * (2 if wl.dtype == "bf16" else 4)
+
+    def fill():
+        B.block_swap(layer.dims, layer.cfg, T, host, cache, sel, cnt, sel, zero, status)
+
+    def empty():
+        B.block_swap(layer.dims, layer.cfg, T, host, cache, sel, zero, sel, cnt, status)
+
+    for _ in range(3):
+        fill()
+        empty()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    total_ms = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fill()
+        e1.record(stream)
+        empty()
+        torch.cuda.synchronize()
+        total_ms += e0.elapsed_time(e1)
+    assert int(status.item()) == 0, "device status set during the block swap"
+    us = total_ms * 1000.0 / reps
+    del hk, hv
+    return {"workload": "one layer's whole selection (every unit) copied into an empty GPU block cache",
+            "bytes_per_call": nbytes, "us_per_call": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "source": "pinned host memory read by the kernel over the host link (unified addressing)"}
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 def max_over_ranks(x: float, device) -> float:
@@ -409,6 +468,8 @@ def run_ours(args) -> None:
     e2e_s = max_over_ranks(e2e_s, dev)
     e2e_value = e2e_s / args.steps * 1e6 / LAYERS
 
+    swap = measure_block_swap(layers[0], wl, B, torch) if rank == 0 else None
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = time_oracle(reps=args.cpu_reps, warm=1)
@@ -426,6 +487,7 @@ def run_ours(args) -> None:
                         "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "kernels_us_per_launch": {k: round(v, 3) for k, v in per_kernel.items()},
+                "block_swap": swap,
                 "algorithmic_bytes_per_layer": nbytes,
                 "layer_step_gbs": round(nbytes["layer_step"] / (value * 1e-6) / 1e9, 1),
                 "layer_step_frac": round(nbytes["layer_step"] / (value * 1e-6) / 1e9 / peak, 4)}

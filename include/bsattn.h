@@ -13,6 +13,8 @@
  *   bs_block_setdiff          blocks added to / removed from the selection since the
  *                             previous step
  *   bs_decode_step            all five for one layer in two launches
+ *   bs_block_swap             moves the blocks that the set-difference adds from host
+ *                             memory into a GPU block cache (the offload path)
  *
  * Method sources: "Technisches Resümee: NOSA: Native und Offloadable Sparse
  * Attention" (section Methodik: "1. Algorithmus: NOSA" and "2. System: NOSI") and
@@ -274,6 +276,63 @@ typedef struct {
  * Errors as for the separate calls; after BS_ERR_TIMEOUT zero the workspace again. */
 bs_status bs_decode_step(const bs_dims *dims, const bs_kv *kv, const bs_head_cfg *cfg, const bs_step_io *io,
                          bs_group_reduce group_reduce, bs_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * Set-difference-driven block swap into a GPU block cache ("Technisches Resümee:
+ * NOSA", Methodik / 2. System: NOSI: the KV cache in minimal block units, set-
+ * difference kernels for block swapping, host-to-device transfer kernels over
+ * Unified Virtual Addressing; Lokalitätsgarantie: blocks kept from one step to the
+ * next stay in the GPU cache).
+ *
+ * The full KV lives in host memory; the GPU holds, per unit, `slots_per_unit` block
+ * slots of `pages_per_slot` pages each (pages_per_slot >= g/16 of every unit). A
+ * block is resident exactly while it is selected: after the swap of a step, the
+ * cached blocks of unit u are that step's selection.
+ * ------------------------------------------------------------------------------ */
+
+/* Host-resident paged KV. The pools must be pinned host memory that the device can
+ * read (under unified addressing the host pointer of cudaHostAlloc / cudaHostRegister
+ * memory is that device pointer); `page_table` is DEVICE memory. */
+typedef struct {
+  const void *k_pool, *v_pool;   /* [n_pages][16][head_dim], kv_dtype, 16-byte aligned */
+  const int32_t *page_table;     /* [units][max_pages_per_unit]: host page of each logical page */
+  int64_t n_pages;
+} bs_host_kv;
+
+/* GPU block cache (all device memory). Slot s of unit u owns device pages
+ * (u * slots_per_unit + s) * pages_per_slot + p, p < pages_per_slot, in `k_pool` and
+ * `v_pool` ([units * slots_per_unit * pages_per_slot][16][head_dim]). `page_table`
+ * ([units][max_pages_per_unit]) maps each logical page of a cached block to its
+ * device page and every other entry to -1; with it and the cache pools, bs_kv
+ * describes the cache for bs_sparse_decode_attn. slot_block / block_slot are the
+ * cache state (in/out; start with all -1). */
+typedef struct {
+  void *k_pool, *v_pool;
+  int32_t *page_table;          /* [units][max_pages_per_unit] */
+  int32_t *slot_block;          /* [units][slots_per_unit]: block held by a slot, -1 free */
+  int32_t *block_slot;          /* [units][max_blocks_per_unit]: slot of a block, -1 not cached */
+  int32_t slots_per_unit;       /* 1..4096, at least the largest selection */
+  int32_t pages_per_slot;       /* >= g/16 of every unit */
+} bs_block_cache;
+
+/* One step's swap for every unit: first every block of `removed` leaves the cache
+ * (its slot is freed, its page-table entries become -1); then the blocks of `added`
+ * (ascending) take the free slots in ascending slot order, their page-table entries
+ * are set, and the pages of each added block that hold tokens (< T) are copied, K and
+ * V, from the host pools into the block's slot (16-byte loads over the host link, no
+ * staging copy). The page holding token T-1 (the token appended this step) is copied
+ * and mapped too when its block was already cached, so the cache stays current as the
+ * tail block grows. `added` / `removed` and their counts are bs_block_setdiff's output
+ * (or bs_decode_step's); seq_lens (device, [batch]) give T. Two launches: the
+ * bookkeeping (one CTA per unit), then the copies (one CTA per added block and one
+ * per unit for the appended token's page).
+ * Device-side errors: a block index outside [0, max_blocks_per_unit) or a host page
+ * outside the host pool sets BS_ERR_DEVICE_BOUNDS (that block is skipped); more added
+ * blocks than free slots sets BS_ERR_CAPACITY (the excess is not cached). */
+bs_status bs_block_swap(const bs_dims *dims, const bs_head_cfg *cfg, const int32_t *seq_lens,
+                        const bs_host_kv *host, const bs_block_cache *cache, const int32_t *added,
+                        const int32_t *added_cnt, const int32_t *removed, const int32_t *removed_cnt,
+                        int32_t *dev_status, bs_stream_t stream);
 
 /* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
 size_t bs_workspace_size(const bs_dims *dims);

@@ -61,6 +61,17 @@ class StepIO(ctypes.Structure):
                 ("dev_status", ctypes.c_void_p)]
 
 
+class HostKV(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("n_pages", ctypes.c_int64)]
+
+
+class BlockCache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("slot_block", ctypes.c_void_p), ("block_slot", ctypes.c_void_p),
+                ("slots_per_unit", ctypes.c_int32), ("pages_per_slot", ctypes.c_int32)]
+
+
 class BsError(RuntimeError):
     def __init__(self, call: str, status: int, text: str):
         super().__init__(f"{call} returned {status} ({text})")
@@ -87,6 +98,9 @@ _SIGS = {
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_decode_step": (ctypes.c_int, [_P(Dims), _P(KV), _P(HeadCfg), _P(StepIO), ctypes.c_int, ctypes.c_void_p]),
+    "bs_block_swap": (ctypes.c_int, [_P(Dims), _P(HeadCfg), ctypes.c_void_p, _P(HostKV), _P(BlockCache),
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -194,6 +208,15 @@ def decode_step(dims, kv, cfg, io: StepIO, group_reduce=BS_GROUP_MAX, stream=Non
     """All five steps of one layer's decode step (two launches)."""
     _check("bs_decode_step", lib().bs_decode_step(ctypes.byref(dims), ctypes.byref(kv), ctypes.byref(cfg),
                                                   ctypes.byref(io), int(group_reduce), _stream(stream)))
+
+
+def block_swap(dims, cfg, seq_lens, host: HostKV, cache: BlockCache, added, added_cnt, removed, removed_cnt,
+               dev_status, stream=None):
+    """Move the blocks the set-difference adds from host memory into the GPU block cache."""
+    _check("bs_block_swap",
+           lib().bs_block_swap(ctypes.byref(dims), ctypes.byref(cfg), _ptr(seq_lens), ctypes.byref(host),
+                               ctypes.byref(cache), _ptr(added), _ptr(added_cnt), _ptr(removed), _ptr(removed_cnt),
+                               _ptr(dev_status), _stream(stream)))
 
 
 def workspace_size(dims) -> int:

@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsattn.so")
 SOURCES = ["bs_api.cu", "bs_summaries.cu", "bs_score.cu", "bs_select.cu", "bs_attn.cu", "bs_attn_bf16.cu",
-           "bs_attn_f32.cu", "bs_setdiff.cu", "bs_step.cu"]
+           "bs_attn_f32.cu", "bs_setdiff.cu", "bs_step.cu", "bs_swap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -22,7 +22,9 @@ What it computes, step by step, in the order and notation of the two method page
 4. softmax attention over only the tokens of the selected blocks (Fluxion,
    "Probleemstelling" item 1: sparse attention over the selected KV blocks);
 5. the set-difference of the selection against the previous step (NOSA,
-   "2. System: NOSI": set-difference kernels for block swapping).
+   "2. System: NOSI": set-difference kernels for block swapping);
+6. the swap that set-difference drives: the bookkeeping of a GPU block cache holding
+   exactly the selected blocks (NOSA, "2. System: NOSI"; "Lokalitätsgarantie").
 
 All arithmetic is float64 on logical (unpaged) arrays; bf16 inputs are widened
 exactly. The pages give no formulas, so where they are silent the plainest reading
@@ -239,6 +241,54 @@ def setdiff(prev, cur):
     """(added, removed) = (cur minus prev, prev minus cur), both ascending."""
     p, c = set(int(x) for x in prev), set(int(x) for x in cur)
     return sorted(c - p), sorted(p - c)
+
+
+# ---------------------------------------------------------------------------
+# 6. Set-difference-driven block swap into a GPU block cache
+# ---------------------------------------------------------------------------
+def block_swap(slot_block, block_slot, added, removed):
+    """One step's cache bookkeeping ("Technisches Resümee: NOSA", Methodik / 2. System:
+    NOSI: the KV cache in minimal block units, set-difference kernels for block
+    swapping; Lokalitätsgarantie: blocks kept between steps stay in the GPU cache).
+
+    slot_block[s] is the block held by slot s (-1 free); block_slot[c] the slot of
+    block c (-1 not cached). Readings where the page is silent: the removed blocks
+    leave first; then the added blocks, in ascending order, take the free slots in
+    ascending slot order; a block is cached exactly while it is selected. Returns the
+    new (slot_block, block_slot) and the (block, slot) pairs whose pages are copied;
+    added blocks beyond the free slots are not placed."""
+    sb = np.array(slot_block, dtype=np.int64).copy()
+    bs = np.array(block_slot, dtype=np.int64).copy()
+    for c in removed:
+        s = int(bs[c])
+        if s >= 0:
+            sb[s] = -1
+        bs[c] = -1
+    free = [s for s in range(sb.size) if sb[s] < 0]
+    copies = []
+    for i, c in enumerate(sorted(int(x) for x in added)):
+        if i >= len(free):
+            break
+        sb[free[i]] = c
+        bs[c] = free[i]
+        copies.append((c, free[i]))
+    return sb, bs, copies
+
+
+def cache_page_table(block_slot, u: int, g: int, T: int, n_row: int, slots: int, pages_per_slot: int):
+    """Page-table row of unit u over the cache: logical page p of a cached block c lies
+    in device page (u * slots + slot) * pages_per_slot + (p - c * g/16) when it holds
+    tokens (16 p < T); every other entry is -1."""
+    ppb = g // 16
+    row = np.full(n_row, -1, dtype=np.int64)
+    for c, s in enumerate(block_slot):
+        if s < 0:
+            continue
+        for j in range(ppb):
+            lp = c * ppb + j
+            if lp < n_row and lp * 16 < T:
+                row[lp] = (u * slots + int(s)) * pages_per_slot + j
+    return row
 
 
 # ---------------------------------------------------------------------------

@@ -112,6 +112,26 @@ def _update_wrong_sub_block(kbar, K, T, s):
     return ORIG["update_sub_block"](kbar, K, T + 1 if T < K.shape[0] else T, s)
 
 
+def _swap_no_free(slot_block, block_slot, added, removed):
+    return ORIG["block_swap"](slot_block, block_slot, added, [])
+
+
+def _swap_highest_slot_first(slot_block, block_slot, added, removed):
+    sb = np.array(slot_block).copy()
+    bs = np.array(block_slot).copy()
+    for c in removed:
+        if bs[c] >= 0:
+            sb[bs[c]] = -1
+        bs[c] = -1
+    free = [s for s in range(sb.size) if sb[s] < 0][::-1]
+    copies = []
+    for n, c in enumerate(sorted(added)):
+        if n < len(free):
+            sb[free[n]], bs[c] = c, free[n]
+            copies.append((c, free[n]))
+    return sb, bs, copies
+
+
 MUTATIONS = {
     "means_divide_by_s": ("sub_block_means", _means_divide_by_s),
     "scores_no_scale": ("block_scores", _scores_no_scale),
@@ -130,6 +150,8 @@ MUTATIONS = {
     "select_gamma_q_overlaps_gamma_e": ("select_unit", _select_gq_overlaps),
     "setdiff_swapped": ("setdiff", _setdiff_swapped),
     "update_wrong_sub_block": ("update_sub_block", _update_wrong_sub_block),
+    "swap_no_free": ("block_swap", _swap_no_free),
+    "swap_highest_slot_first": ("block_swap", _swap_highest_slot_first),
 }
 
 ORIG = {name: getattr(O, name) for name, _ in MUTATIONS.values()}

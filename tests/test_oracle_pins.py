@@ -344,10 +344,57 @@ def check_p10_incremental(orc):
         np.testing.assert_array_equal(orc.sub_block_means(Kc, 23, s), 2.5)
 
 
+def check_golden_block_swap(orc):
+    gd = _golden.load("block_swap.txt")
+    slots, blocks, g, u = _golden.i(gd["slots"]), _golden.i(gd["blocks"]), _golden.i(gd["g"]), _golden.i(gd["u"])
+    sb, bs = np.full(slots, -1), np.full(blocks, -1)
+    prev = []
+    for step in (1, 2, 3):
+        sel = _golden.ints(gd[f"s{step}.sel"])
+        added, removed = orc.setdiff(prev, sel)
+        sb, bs, copies = orc.block_swap(sb, bs, added, removed)
+        assert _golden.ints(sb) == _golden.ints(gd[f"s{step}.slot_block"]), step
+        exp = np.atleast_2d(gd[f"s{step}.copies"]).astype(int).tolist()
+        assert [list(c) for c in copies] == exp, step
+        prev = sel
+    row = orc.cache_page_table(bs, u, g, _golden.i(gd["s3.T"]), 20, slots, 2)
+    assert _golden.ints(row) == _golden.ints(gd["s3.page_table"])
+
+
+def check_p11_block_swap_invariants(orc):
+    """Over random selection sequences the cache holds exactly the selection, slots and
+    blocks map one to one, each added block is copied once and a kept block never
+    moves (no re-copy: the point of the locality guarantee)."""
+    rng = np.random.default_rng(19)
+    for trial in range(30):
+        n_blocks, cap = int(rng.integers(5, 60)), int(rng.integers(1, 12))
+        sb, bs = np.full(cap, -1), np.full(n_blocks, -1)
+        prev = []
+        for _ in range(12):
+            keep = [c for c in prev if rng.random() < 0.7]
+            fresh = [int(c) for c in rng.choice(n_blocks, size=int(rng.integers(0, min(cap, n_blocks) + 1)),
+                                                replace=False)]
+            sel = sorted(set(keep) | set(fresh))[:cap]
+            added, removed = orc.setdiff(prev, sel)
+            before = bs.copy()
+            sb, bs, copies = orc.block_swap(sb, bs, added, removed)
+            cached = sorted(int(c) for c in np.flatnonzero(bs >= 0))
+            assert cached == sel
+            for s, c in enumerate(sb):
+                if c >= 0:
+                    assert bs[c] == s
+            assert sorted(c for c, _ in copies) == added
+            for c in sel:
+                if c in prev:
+                    assert bs[c] == before[c]
+            prev = sel
+
+
 ALL_CHECKS = [check_golden_pooling, check_golden_select_retrieval, check_golden_select_dual,
               check_golden_attention, check_p1_full_budget_is_dense, check_p2_streaming_is_sink_window,
               check_p3_select_brute_force, check_p4_p5_eviction, check_p6_pooling_special_cases,
-              check_p7_setdiff, check_p8_planted, check_p9_lse_merge, check_p10_incremental]
+              check_p7_setdiff, check_p8_planted, check_p9_lse_merge, check_p10_incremental,
+              check_golden_block_swap, check_p11_block_swap_invariants]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
