@@ -289,6 +289,57 @@ def measure_block_swap(layer, wl, B, torch, reps: int = 20) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# CPU/GPU split attention: the host cores' share and the GPU merge
+# ---------------------------------------------------------------------------
+def measure_cpu_split(layer, wl, B, torch, reps: int = 10) -> dict:
+    """Time bs_cpu_sparse_attn on every other selected block of every unit (about half
+    the layer's selected KV, read from host memory by all host cores) and bs_lse_merge
+    combining its result with a GPU partial result."""
+    import numpy as np
+    dev = layer.device
+    lists = layer.selection(0)
+    MS = layer.max_sel
+    idx = np.full((wl.U, MS), -1, np.int32)
+    cnt = np.zeros(wl.U, np.int32)
+    for u, lst in enumerate(lists):
+        part = lst[1::2]
+        idx[u, :len(part)] = part
+        cnt[u] = len(part)
+    hk, hv = layer.k_pool.cpu(), layer.v_pool.cpu()
+    pt, seq, gs = layer.page_table.cpu(), layer.seq_lens[0].cpu(), layer.cfg_arrays["block_tokens"].cpu()
+    qh = layer.q[0].cpu()
+    out = np.zeros((wl.B, wl.Hq, wl.d), np.float32)
+    lse = np.zeros((wl.B, wl.Hq), np.float32)
+    host = B.HostKV(k_pool=hk.data_ptr(), v_pool=hv.data_ptr(), page_table=0, n_pages=int(wl.n_pages))
+    tables = B.HostTables(page_table=pt.data_ptr(), seq_lens=seq.data_ptr(), block_tokens=gs.data_ptr())
+    threads = os.cpu_count() or 1
+    Tn = [int(wl.T(0, u // wl.Hkv)) for u in range(wl.U)]
+    tokens = sum(min(int(wl.g[u]), Tn[u] - c * int(wl.g[u])) for u in range(wl.U) for c in idx[u, :cnt[u]])
+    nbytes = tokens * 2 * wl.d * (2 if wl.dtype == "bf16" else 4)
+    B.cpu_sparse_attn(layer.dims, qh, host, tables, idx, cnt, out, lse, threads)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        B.cpu_sparse_attn(layer.dims, qh, host, tables, idx, cnt, out, lse, threads)
+        times.append(time.perf_counter() - t0)
+    cpu_us = statistics.median(times) * 1e6
+    ob, lb = torch.as_tensor(out, device=dev), torch.as_tensor(lse, device=dev)
+    oa, la = layer.out.clone(), layer.lse.clone()
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        B.lse_merge(layer.dims, oa, la, ob, lb, oa, la)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(100):
+        B.lse_merge(layer.dims, oa, la, ob, lb, oa, la)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return {"cpu_share": "every other selected block of every unit", "cpu_bytes": nbytes, "cpu_threads": threads,
+            "cpu_us": round(cpu_us, 1), "cpu_gbs": round(nbytes / (cpu_us * 1e-6) / 1e9, 2),
+            "merge_us": round(e0.elapsed_time(e1) * 10.0, 3)}
+
+
+# ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
 def max_over_ranks(x: float, device) -> float:
@@ -469,6 +520,7 @@ def run_ours(args) -> None:
     e2e_value = e2e_s / args.steps * 1e6 / LAYERS
 
     swap = measure_block_swap(layers[0], wl, B, torch) if rank == 0 else None
+    split = measure_cpu_split(layers[0], wl, B, torch) if rank == 0 else None
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -488,6 +540,7 @@ def run_ours(args) -> None:
                 "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "kernels_us_per_launch": {k: round(v, 3) for k, v in per_kernel.items()},
                 "block_swap": swap,
+                "cpu_gpu_split": split,
                 "algorithmic_bytes_per_layer": nbytes,
                 "layer_step_gbs": round(nbytes["layer_step"] / (value * 1e-6) / 1e9, 1),
                 "layer_step_frac": round(nbytes["layer_step"] / (value * 1e-6) / 1e9 / peak, 4)}

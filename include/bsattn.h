@@ -15,6 +15,8 @@
  *   bs_decode_step            all five for one layer in two launches
  *   bs_block_swap             moves the blocks that the set-difference adds from host
  *                             memory into a GPU block cache (the offload path)
+ *   bs_cpu_sparse_attn,       attention of a block subset on the host cores, and the
+ *   bs_lse_merge              GPU merge of two partial results (CPU/GPU split)
  *
  * Method sources: "Technisches Resümee: NOSA: Native und Offloadable Sparse
  * Attention" (section Methodik: "1. Algorithmus: NOSA" and "2. System: NOSI") and
@@ -333,6 +335,42 @@ bs_status bs_block_swap(const bs_dims *dims, const bs_head_cfg *cfg, const int32
                         const bs_host_kv *host, const bs_block_cache *cache, const int32_t *added,
                         const int32_t *added_cnt, const int32_t *removed, const int32_t *removed_cnt,
                         int32_t *dev_status, bs_stream_t stream);
+
+/* ------------------------------------------------------------------------------
+ * CPU/GPU split attention ("Technische Samenvatting: Fluxion", Kerninzichten item 3:
+ * sparse attention is bound by data movement; Systeemcomponenten: the CPU and the GPU
+ * serve one step in parallel). A unit's selection may be split into two block subsets:
+ * one attended on the GPU (bs_sparse_decode_attn, e.g. over the block cache), the
+ * other on the host cores over host-resident KV (bs_cpu_sparse_attn); bs_lse_merge
+ * combines the two partial results into the attention over the union.
+ * ------------------------------------------------------------------------------ */
+
+/* Host copies of the tables the CPU side reads (all HOST memory). */
+typedef struct {
+  const int32_t *page_table;    /* [units][max_pages_per_unit]: host page of each logical page */
+  const int32_t *seq_lens;      /* [batch]: T */
+  const int32_t *block_tokens;  /* [units]: g */
+} bs_host_tables;
+
+/* Attention of each unit's listed blocks (tokens clipped to T) on the host cores,
+ * fp32 arithmetic, units spread over n_threads threads; synchronous. Everything is
+ * HOST memory: q ([batch][n_q_heads][head_dim], q_dtype), the pools of `kv` (its
+ * page_table field is not used; `tables` gives the host page table), sel_idx
+ * ([units][max_sel_per_unit], ascending), sel_cnt ([units]), out ([batch][n_q_heads]
+ * [head_dim] fp32) and lse ([batch][n_q_heads] fp32, natural log; -inf and a zero row
+ * for a unit with nothing to attend). Returns BS_ERR_DEVICE_BOUNDS (after finishing
+ * the other units) if a block or page index is out of range. */
+bs_status bs_cpu_sparse_attn(const bs_dims *dims, const void *q, const bs_host_kv *kv, const bs_host_tables *tables,
+                             const int32_t *sel_idx, const int32_t *sel_cnt, float *out, float *lse,
+                             int n_threads);
+
+/* out, lse = the log-sum-exp merge of two partial attention results over disjoint
+ * token sets of every query head (device memory, layout of out / lse above): with
+ * M = max(lse_a, lse_b), w = exp(lse - M), out = (w_a o_a + w_b o_b) / (w_a + w_b) and
+ * lse = M + log(w_a + w_b); a side with lse = -inf contributes nothing, and two
+ * empty sides give a zero row and -inf. out / lse may be out_a / lse_a (in place). */
+bs_status bs_lse_merge(const bs_dims *dims, const float *out_a, const float *lse_a, const float *out_b,
+                       const float *lse_b, float *out, float *lse, bs_stream_t stream);
 
 /* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
 size_t bs_workspace_size(const bs_dims *dims);

@@ -72,6 +72,10 @@ class BlockCache(ctypes.Structure):
                 ("slots_per_unit", ctypes.c_int32), ("pages_per_slot", ctypes.c_int32)]
 
 
+class HostTables(ctypes.Structure):
+    _fields_ = [("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("block_tokens", ctypes.c_void_p)]
+
+
 class BsError(RuntimeError):
     def __init__(self, call: str, status: int, text: str):
         super().__init__(f"{call} returned {status} ({text})")
@@ -101,6 +105,10 @@ _SIGS = {
     "bs_block_swap": (ctypes.c_int, [_P(Dims), _P(HeadCfg), ctypes.c_void_p, _P(HostKV), _P(BlockCache),
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_void_p, ctypes.c_void_p]),
+    "bs_cpu_sparse_attn": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, _P(HostKV), _P(HostTables), ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
+    "bs_lse_merge": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
@@ -217,6 +225,19 @@ def block_swap(dims, cfg, seq_lens, host: HostKV, cache: BlockCache, added, adde
            lib().bs_block_swap(ctypes.byref(dims), ctypes.byref(cfg), _ptr(seq_lens), ctypes.byref(host),
                                ctypes.byref(cache), _ptr(added), _ptr(added_cnt), _ptr(removed), _ptr(removed_cnt),
                                _ptr(dev_status), _stream(stream)))
+
+
+def cpu_sparse_attn(dims, q, kv: HostKV, tables: HostTables, sel_idx, sel_cnt, out, lse, n_threads: int):
+    """Attention of the listed blocks on the host cores (every buffer in host memory)."""
+    _check("bs_cpu_sparse_attn",
+           lib().bs_cpu_sparse_attn(ctypes.byref(dims), _ptr(q), ctypes.byref(kv), ctypes.byref(tables),
+                                    _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), int(n_threads)))
+
+
+def lse_merge(dims, out_a, lse_a, out_b, lse_b, out, lse, stream=None):
+    """Merge two partial attention results over disjoint token sets (device memory)."""
+    _check("bs_lse_merge", lib().bs_lse_merge(ctypes.byref(dims), _ptr(out_a), _ptr(lse_a), _ptr(out_b),
+                                              _ptr(lse_b), _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def workspace_size(dims) -> int:

@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libbsattn.so")
 SOURCES = ["bs_api.cu", "bs_summaries.cu", "bs_score.cu", "bs_select.cu", "bs_attn.cu", "bs_attn_bf16.cu",
-           "bs_attn_f32.cu", "bs_setdiff.cu", "bs_step.cu", "bs_swap.cu"]
+           "bs_attn_f32.cu", "bs_setdiff.cu", "bs_step.cu", "bs_swap.cu", "bs_split.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
@@ -54,7 +54,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
