@@ -210,8 +210,8 @@ def _measured_traffic(kernel: str, workload: str):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
-    rec = json.load(open(p)).get(kernel)
-    if not rec or rec.get("workload") != workload or rec.get("csrc_sha") != csrc_sha():
+    rec = json.load(open(p)).get(kernel, {}).get(workload)
+    if not rec or rec.get("csrc_sha") != csrc_sha():
         return None
     return rec["bytes_per_launch"]
 
