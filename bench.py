@@ -194,6 +194,13 @@ def algorithmic_bytes(wl, sel_lists, prev_lists):
     return out
 
 
+def _json_default(o):
+    """numpy scalars in the JSON line become plain numbers."""
+    if hasattr(o, "item"):
+        return o.item()
+    raise TypeError(f"not JSON serializable: {type(o).__name__}")
+
+
 def csrc_sha() -> str:
     """Hash of every CUDA source and header of the library (any change invalidates counters)."""
     d = os.path.join(ROOT, "long_context_serving_gb300", "csrc")
@@ -257,8 +264,8 @@ def measure_block_swap(layer, wl, B, torch, reps: int = 20) -> dict:
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     lists = layer.selection(0)
     Tn = [int(wl.T(0, u // wl.Hkv)) for u in range(U)]
-    pages = sum(-(-min(int(wl.g[u]), Tn[u] - c * int(wl.g[u])) // PAGE) for u in range(U) for c in lists[u])
-    nbytes = pages * 2 * PAGE * wl.d * (2 if wl.dtype == "bf16" else 4)
+    pages = sum(-(-min(int(wl.g[u]), Tn[u] - int(c) * int(wl.g[u])) // PAGE) for u in range(U) for c in lists[u])
+    nbytes = int(pages) * 2 * PAGE * int(wl.d) * (2 if wl.dtype == "bf16" else 4)
 
     def fill():
         B.block_swap(layer.dims, layer.cfg, T, host, cache, sel, cnt, sel, zero, status)
@@ -314,8 +321,8 @@ def measure_cpu_split(layer, wl, B, torch, reps: int = 10) -> dict:
     tables = B.HostTables(page_table=pt.data_ptr(), seq_lens=seq.data_ptr(), block_tokens=gs.data_ptr())
     threads = os.cpu_count() or 1
     Tn = [int(wl.T(0, u // wl.Hkv)) for u in range(wl.U)]
-    tokens = sum(min(int(wl.g[u]), Tn[u] - c * int(wl.g[u])) for u in range(wl.U) for c in idx[u, :cnt[u]])
-    nbytes = tokens * 2 * wl.d * (2 if wl.dtype == "bf16" else 4)
+    tokens = sum(min(int(wl.g[u]), Tn[u] - int(c) * int(wl.g[u])) for u in range(wl.U) for c in idx[u, :cnt[u]])
+    nbytes = int(tokens) * 2 * int(wl.d) * (2 if wl.dtype == "bf16" else 4)
     B.cpu_sparse_attn(layer.dims, qh, host, tables, idx, cnt, out, lse, threads)
     times = []
     for _ in range(reps):
@@ -544,7 +551,7 @@ def run_ours(args) -> None:
                 "algorithmic_bytes_per_layer": nbytes,
                 "layer_step_gbs": round(nbytes["layer_step"] / (value * 1e-6) / 1e9, 1),
                 "layer_step_frac": round(nbytes["layer_step"] / (value * 1e-6) / 1e9 / peak, 4)}
-        print(json.dumps(line), flush=True)
+        print(json.dumps(line, default=_json_default), flush=True)
     if world > 1:
         dist.destroy_process_group()
 

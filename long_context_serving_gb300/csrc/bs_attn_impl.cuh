@@ -61,6 +61,18 @@ __device__ __forceinline__ int load_relaxed_gpu(const int32_t *p) {
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Starts pulling unit u's page-table row into L2 (one 128-byte line per thread) while
+// the block list is read, so the page lookups that follow hit L2. Skipped when the
+// fused step hands the attention its pages ready in a page list.
+template <int NT>
+__device__ __forceinline__ void prefetch_page_row(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
+                                                  const int32_t *plist, int u, bool in_step) {
+  if (plist != nullptr && in_step && cfg.cls[u] != BS_STREAMING) return;
+  const int32_t *row = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+  const int lines = (dims.max_pages_per_unit + 31) / 32;
+  for (int i = threadIdx.x; i < lines; i += NT) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + i * 32));
+}
+
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *p, int v) {
   int old;
   asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -495,6 +507,7 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
+  prefetch_page_row<NT>(dims, kv, cfg, plist, u, in_step);
   const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);
@@ -774,6 +787,7 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
+  prefetch_page_row<NT>(dims, kv, cfg, plist, u, in_step);
   const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
   if (!ub.ok || ub.pg.n_pages == 0) {
     write_empty_output<NT, D, G>(out, lse, orow0);

@@ -145,6 +145,8 @@ class PagedLayer:
     def prefill(self, stream=None) -> None:
         """Summaries of every prefilled token."""
         max_new = int(self.wl.T_prefill.max())
+        if max_new == 0:       # an empty cache: the first decode step's update covers token 0
+            return
         B.build_block_summaries(self.dims, self.kv_at(self.prefill_lens), self.cfg, self.zeros_b, max(max_new, 1),
                                 self.summaries, self.status, stream)
 

@@ -98,6 +98,39 @@ def test_parity_few_splits_per_unit(B, fused):
     rep.check()
 
 
+@pytest.mark.parametrize("T", [1, 17, 40])
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_tiny_lengths(T, fused):
+    """One token, a partial first block, a budget larger than the candidates."""
+    rep = run_parity(make_workload(2, seed=15, T=T), fused=fused)
+    rep.check()
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_degenerate_budgets(fused):
+    """Dual units with k = 0 (forced blocks only), k_e = k (no query-aware blocks) and
+    k_e = 0 (no eviction-driven blocks)."""
+    wl = make_workload(5, seed=16, B=2, T=3000, steps=3)
+    wl.k[0::2] = 0
+    wl.k_e[0::2] = 0
+    wl.k_e[1::4] = wl.k[1::4]
+    wl.k_e[3::4] = 0
+    rep = run_parity(wl, fused=fused)
+    rep.check()
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_shared_memory_selection_path(fused):
+    """More candidates than the register path holds (9,374 blocks of 16 tokens)."""
+    wl = make_workload(3, seed=17, B=1, T=150000, steps=1)
+    wl.g[:] = 16
+    wl.s[:] = 4
+    wl.cls[:] = O.RETRIEVAL
+    wl.k[:] = 300
+    rep = run_parity(wl, units=[0, 5], summary_rows_sample=256, fused=fused)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
