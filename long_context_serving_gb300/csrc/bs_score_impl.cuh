@@ -4,8 +4,9 @@
 // at block level), shared by the query heads of a GQA group ("Technische Samenvatting:
 // Fluxion", Systeemcomponenten, "Granularity-Budget Selector").
 //
-// One CTA of 256 threads scores a tile of 64 consecutive summary rows (64/r whole
-// blocks, r = g/s). The tile arrives in shared memory with one bulk copy. Each warp
+// A CTA of 256 threads scores tiles of 64 consecutive summary rows (64/r whole
+// blocks, r = g/s), each arriving in shared memory with one bulk copy (two buffers
+// when a CTA takes several tiles: the next tile's copy flies during this one). Each warp
 // takes 8 rows; each lane keeps its slice of the G query vectors (pre-scaled by
 // 1/sqrt(d)) in registers and reads its slice of every row once, and a butterfly
 // reduce-scatter across the lanes completes the dot products: shared memory is read
@@ -23,9 +24,12 @@ constexpr int kTileRows = 64;
 
 template <int D, int G>
 struct ScoreLayout {
-  static constexpr int kOffQ = kTileRows * D * 4;
-  static constexpr int kOffDots = kOffQ + G * D * 4;
-  static constexpr int kBytes = kOffDots + kTileRows * G * 4;
+  static constexpr int kTileBytes = kTileRows * D * 4;
+  // nb tile buffers, then the G query vectors [G][D] and the dot products [64][G].
+  __host__ __device__ static constexpr int off_q(int nb) { return nb * kTileBytes; }
+  __host__ __device__ static constexpr int off_dots(int nb) { return off_q(nb) + G * D * 4; }
+  __host__ __device__ static constexpr int bytes(int nb) { return off_dots(nb) + kTileRows * G * 4; }
+  static constexpr int kBytes = kTileRows * D * 4 + G * D * 4 + kTileRows * G * 4;  // one buffer
 };
 
 // Blocks of a unit's candidate range covered by one tile, and the tile count.
@@ -35,60 +39,64 @@ __host__ __device__ __forceinline__ int score_tiles(const Geom &ge) {
   return (ge.c_hi - ge.c_lo + bpt - 1) / bpt;
 }
 
-// Starts the bulk copy of summary rows [row0, min(row0 + 64, row_end)) of a unit
-// (summ_unit: its first row, 16-byte aligned) into the tile buffer and returns the row
-// count (0: nothing in flight). The barrier is initialised either way; every thread
-// calls it, and every thread must call score_tile_finish afterwards, which waits for
-// the copy, before the shared memory is reused or the CTA exits.
-template <int D, int G>
-__device__ __forceinline__ int score_tile_issue(const float *summ_unit, int64_t row0, int64_t row_end,
-                                                unsigned char *smem, uint64_t *bar) {
+// Thread 0 initialises nb copy barriers; the caller synchronises before their use.
+__device__ __forceinline__ void score_bars_init(uint64_t *bars, int nb) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nb; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+}
+
+// Starts (thread 0) the bulk copy of summary rows [row0, min(row0 + 64, row_end)) of a
+// unit (summ_unit: its first row, 16-byte aligned) into `buf` on barrier `bar` and
+// returns the row count to every thread (0: nothing in flight).
+template <int D>
+__device__ __forceinline__ int score_copy(const float *summ_unit, int64_t row0, int64_t row_end, void *buf,
+                                          uint64_t *bar) {
   const int64_t left = row_end - row0;
   const int n = row0 < 0 ? 0 : static_cast<int>(left < kTileRows ? (left > 0 ? left : 0) : kTileRows);
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    if (n > 0) {
-      const uint32_t bytes = static_cast<uint32_t>(n) * D * sizeof(float);
-      mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(smem, summ_unit + row0 * D, bytes, bar);
-    }
+  if (threadIdx.x == 0 && n > 0) {
+    const uint32_t bytes = static_cast<uint32_t>(n) * D * sizeof(float);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(buf, summ_unit + row0 * D, bytes, bar);
   }
-  __syncthreads();
   return n;
 }
 
-// Waits for the copy started by score_tile_issue (n_loaded rows) and, if `score`,
-// scores tile `tile` of the unit's candidates into row_out[c] (c = block index): the
-// copied rows must start at row c_lo * r + 64 * tile and cover the tile. qrow points at
-// the unit's G query vectors. Returns false when the copy timed out. All 256 threads
-// call it with the same arguments.
+// The G query vectors of the unit, pre-scaled by 1/sqrt(d), into shared memory.
 template <int D, int G>
-__device__ bool score_tile_finish(int n_loaded, bool score, const void *qrow, int q_dtype, const Geom &ge, int tile,
-                                  int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
-  using L = ScoreLayout<D, G>;
-  float *tile_sm = reinterpret_cast<float *>(smem);          // [64][D]
-  float *qs = reinterpret_cast<float *>(smem + L::kOffQ);     // [G][D]
-  float *dots = reinterpret_cast<float *>(smem + L::kOffDots);  // [64][G]
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void score_load_q(float *qs, const void *qrow, int q_dtype) {
   const float scale = rsqrtf(static_cast<float>(D));
-  if (score)
-    for (int i = tid; i < G * D; i += kScoreThreads) qs[i] = load_scalar(qrow, i, q_dtype) * scale;
-  const bool ok = n_loaded == 0 || mbar_wait_bounded(bar, 0, st);
-  if (__syncthreads_or(!ok)) return false;
-  if (!score) return true;
+  for (int i = threadIdx.x; i < G * D; i += kScoreThreads) qs[i] = load_scalar(qrow, i, q_dtype) * scale;
+}
+
+// Waits for a copy of n_loaded rows on `bar` (phase `parity`); false (for every
+// thread) when it timed out. All threads call it.
+__device__ __forceinline__ bool score_wait(uint64_t *bar, uint32_t parity, int n_loaded, int32_t *st) {
+  const bool ok = n_loaded == 0 || mbar_wait_bounded(bar, parity, st);
+  return !__syncthreads_or(!ok);
+}
+
+// Scores tile `tile` of the unit's candidates from `tile_sm` (rows from c_lo * r + 64 *
+// tile, n_loaded of them, covering the tile) into row_out[c] (c = block index). qs holds
+// the scaled queries (visible to all threads). All 256 threads call it; the tile buffer
+// is no longer read when it returns.
+//
+// Dot products: warp w takes rows 8w .. 8w+7 of the tile; lane l owns dimensions
+// [l*DPL, (l+1)*DPL) and keeps the G query slices of them in registers, so shared
+// memory is read once per row (a contiguous row per warp). Each lane forms the 8 x G
+// partial sums of its dimensions; a butterfly reduce-scatter over the 32 lanes (values
+// halved at each of 5 stages) leaves lane l with the full sums of entries
+// [l*NF, (l+1)*NF) of the row-major (row, head) list.
+template <int D, int G>
+__device__ void score_compute(const float *tile_sm, const float *qs, float *dots, const Geom &ge, int tile,
+                              int reduce, int n_loaded, float *row_out) {
+  const int tid = threadIdx.x;
   const int r = ge.g / ge.s;
   const int bpt = kTileRows / r;
   const int c_first = ge.c_lo + tile * bpt;
   const int nb = min(bpt, ge.c_hi - c_first);
   const int nrows = min(nb * r, n_loaded);
-
-  // Dot products. Warp w takes rows 8w .. 8w+7 of the tile; lane l owns dimensions
-  // [l*DPL, (l+1)*DPL) and keeps the G query slices of them in registers, so shared
-  // memory is read once per row (a contiguous row per warp). Each lane forms the
-  // 8 x G partial sums of its dimensions; a butterfly reduce-scatter over the 32
-  // lanes (values halved at each of 5 stages) leaves lane l with the full sums of
-  // entries [l*NF, (l+1)*NF) of the row-major (row, head) list.
   static_assert(D % 32 == 0 && D / 32 <= 4, "head_dim 32..128");
   constexpr int DPL = D / 32;
   constexpr int GP = G <= 4 ? 4 : 8;  // heads padded to a power of two
@@ -166,23 +174,31 @@ __device__ bool score_tile_finish(int n_loaded, bool score, const void *qrow, in
     if (reduce != BS_GROUP_MAX) red = red / static_cast<float>(G);
     row_out[c_first + tid] = red;
   }
-  return true;
+  __syncthreads();  // dots are free again
 }
 
-// Scores tile `tile` of a unit's candidates into row_out[c] (c = block index).
-// summ_unit points at the unit's first summary row (16-byte aligned); qrow at its G
-// query vectors. Returns false when the bulk copy timed out. All 256 threads call it
-// with the same arguments; the tile must exist.
+// Scores tile `tile` of a unit's candidates into row_out[c] (c = block index), one
+// buffer. summ_unit points at the unit's first summary row (16-byte aligned); qrow at
+// its G query vectors. Returns false when the bulk copy timed out. All 256 threads
+// call it with the same arguments; the tile must exist.
 template <int D, int G>
 __device__ bool score_tile(const float *summ_unit, const void *qrow, int q_dtype, const Geom &ge, int tile,
                            int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
+  using L = ScoreLayout<D, G>;
   const int r = ge.g / ge.s;
   const int bpt = kTileRows / r;
   const int c_first = ge.c_lo + tile * bpt;
   const int nb = min(bpt, ge.c_hi - c_first);
   const int64_t row0 = static_cast<int64_t>(c_first) * r;
-  const int n = score_tile_issue<D, G>(summ_unit, row0, row0 + nb * r, smem, bar);
-  return score_tile_finish<D, G>(n, true, qrow, q_dtype, ge, tile, reduce, row_out, smem, bar, st);
+  score_bars_init(bar, 1);
+  __syncthreads();
+  const int n = score_copy<D>(summ_unit, row0, row0 + nb * r, smem, bar);
+  float *qs = reinterpret_cast<float *>(smem + L::off_q(1));
+  score_load_q<D, G>(qs, qrow, q_dtype);
+  if (!score_wait(bar, 0, n, st)) return false;
+  score_compute<D, G>(reinterpret_cast<const float *>(smem), qs, reinterpret_cast<float *>(smem + L::off_dots(1)),
+                      ge, tile, reduce, n, row_out);
+  return true;
 }
 
 }  // namespace bsi

@@ -1,21 +1,24 @@
 // The fused decode step of one layer: all five steps of the path in two launches.
 //
-// Launch 1, step_front_kernel, one CTA per (unit, score tile), tile-major:
-//   * every tile of a retrieval or dual unit scores its candidate blocks (a2); tile 0
-//     also recomputes the sub-block holding the token just appended (a1). That
-//     sub-block lies in the always-forced tail block, which no score of this step
-//     reads, so a1 runs beside a2;
-//   * the last tile of each unit to finish (an integer arrival ticket, one acquire-
-//     release atomic per CTA) selects the unit's blocks (a3), publishes the selection
-//     (its count is written last, with a release store) and writes its set-difference
-//     against the previous step (a5);
-//   * a streaming unit has one tile that does a1, a3 and a5.
+// Launch 1, step_front_kernel, one CTA per (unit, group of score tiles), unit-fastest:
+//   * the CTAs of a retrieval or dual unit score its candidate blocks (a2), one or
+//     several 64-row tiles each; the unit's first CTA also recomputes the sub-block
+//     holding the token just appended (a1). That sub-block lies in the always-forced
+//     tail block, which no score of this step reads, so a1 runs beside a2;
+//   * the last CTA of each unit to finish (an integer arrival ticket, one acquire-
+//     release atomic per CTA) selects the unit's blocks (a3), writes the page list of
+//     the selection for the attention, publishes the selection (its count is written
+//     last, with a release store) and writes its set-difference against the previous
+//     step (a5);
+//   * a streaming unit has one CTA that does a1, a3 and a5.
 // Launch 2, the attention (a4) as a programmatic dependent launch: streaming units'
 // splits need no selection and start while launch 1 is still working; every other
 // unit's splits wait (bounded) until their unit's selection count is published.
 //
 // Both kernels are programmatic dependents of the work before them in the stream: they
 // read only the per-unit head configuration before waiting for it to finish.
+#include <algorithm>
+
 #include "bs_attn_launch.cuh"
 #include "bs_score_impl.cuh"
 #include "bs_select_impl.cuh"
@@ -58,14 +61,18 @@ __host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel
 template <int D, int G>
 __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
                                                                    bs_step_io io, int reduce, int32_t *arrivals,
-                                                                   int32_t *plist, int pt_cache_ints) {
+                                                                   int32_t *plist, int pt_cache_ints, int tpc) {
+  using L = ScoreLayout<D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bars[2];
   __shared__ SelShared<kFrontThreads> sh;
   __shared__ int is_last;
-  const int u = blockIdx.x, tile = blockIdx.y, tid = threadIdx.x;  // tile-major: every unit's tile 0 first
+  // CTA j of unit u scores tiles [j * tpc, (j + 1) * tpc); grid is unit-fastest so every
+  // unit's first CTA comes first.
+  const int u = blockIdx.x, cj = blockIdx.y, tid = threadIdx.x;
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const int MB = dims.max_blocks_per_unit, MS = dims.max_sel_per_unit;
+  const int nbuf = tpc > 1 ? 2 : 1;
   int32_t *st = io.dev_status;
   // Per-unit head configuration: read before the preceding work has finished.
   const int cls = cfg.cls[u], g = cfg.block_tokens[u], s = cfg.sub_tokens[u];
@@ -74,27 +81,42 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   const int rows = cfg.sum_rows[u];
   const bool cfg_ok = unit_cfg_ok(cls, g, s, k, k_e, sink, local);
   const bool scored = cfg_ok && cls != BS_STREAMING;
-  // First summary row of this tile: candidates start after the sink blocks (the checks
+  // First summary row of tile t: candidates start after the sink blocks (the checks
   // below confirm this once the length is known; otherwise the unit has no candidates).
-  const int64_t row0 =
-      scored ? static_cast<int64_t>((sink + g - 1) / g) * (g / s) + static_cast<int64_t>(tile) * kTileRows : -1;
+  const int64_t row_base = scored ? static_cast<int64_t>((sink + g - 1) / g) * (g / s) : -1;
+  auto tile_row = [&](int t) -> int64_t { return scored ? row_base + static_cast<int64_t>(t) * kTileRows : -1; };
+  const int t0 = cj * tpc;
   // CTAs past every tile the unit can have leave before waiting.
-  if (tile > 0 && (!scored || row0 >= rows)) return;
+  if (cj > 0 && (!scored || tile_row(t0) >= rows)) return;
   pdl_wait_front();  // q, lengths, KV pages, summaries and selection state are now final
   // The attention reads a non-streaming unit's selection once its count is >= 0: mark
   // it not ready before any attention CTA can start (the buffer's last readers, the
   // previous step, have finished).
-  if (tile == 0 && tid == 0) {
+  if (cj == 0 && tid == 0) {
     io.cur_cnt[u] = -1;
     __threadfence();
   }
+  score_bars_init(bars, nbuf);
   __syncthreads();
   pdl_trigger_front();  // the attention may start launching
-  // Start this tile's summary copy before reading the length (every path below waits
-  // for it in score_tile_finish before returning).
+  // Start the copies of this CTA's first tiles before reading the length; every path
+  // below waits for whatever is in flight (drain) before returning or reusing memory.
   const bool spec = scored && off >= 0 && off % 4 == 0;
-  const int n_loaded = score_tile_issue<D, G>(io.summaries + (spec ? off : 0), spec ? row0 : -1, rows, smem, &bar);
-  const Geom none{};
+  const float *summ = io.summaries + (spec ? off : 0);
+  int inflight[2] = {0, 0}, uses[2] = {0, 0};
+  for (int i = 0; i < nbuf && i < tpc; ++i)
+    inflight[i] = score_copy<D>(summ, spec ? tile_row(t0 + i) : -1, rows, smem + i * L::kTileBytes, &bars[i]);
+  auto wait_buf = [&](int i) -> bool {
+    const bool ok = score_wait(&bars[i], static_cast<uint32_t>(uses[i] & 1), inflight[i], st);
+    if (inflight[i] > 0) ++uses[i];
+    inflight[i] = 0;
+    return ok;
+  };
+  auto drain = [&]() -> bool {
+    bool ok = true;
+    for (int i = 0; i < nbuf; ++i) ok = wait_buf(i) && ok;
+    return ok;
+  };
 
   const int T = kv.seq_lens[b];
   const size_t srow = static_cast<size_t>(u) * MS;
@@ -106,8 +128,8 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
     code = BS_ERR_CAPACITY;
   else if (off % 4 != 0) code = BS_ERR_ALIGN;
   if (code != BS_OK) {
-    score_tile_finish<D, G>(n_loaded, false, nullptr, 0, none, 0, reduce, nullptr, smem, &bar, st);
-    if (tile == 0) {
+    drain();
+    if (cj == 0) {
       for (int i = tid; i < MS; i += kFrontThreads) io.cur_idx[srow + i] = io.added[srow + i] = io.removed[srow + i] = -1;
       __syncthreads();
       if (tid == 0) {
@@ -122,19 +144,36 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   const Geom ge = unit_geom(T, g, s, sink, local);
   int n_tiles = 1;
   if (cls != BS_STREAMING) n_tiles = max(1, score_tiles(ge));
+  const int n_ctas = (n_tiles + tpc - 1) / tpc;  // CTAs of this unit that take part
   float *score_row = io.scores + static_cast<size_t>(u) * MB;
   // Scored only when the candidates exist, in which case they start at the sink's end
-  // and the rows copied above are this tile's.
-  const bool score = cls != BS_STREAMING && ge.c_hi > ge.c_lo && tile < n_tiles;
-  const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
-  const void *qrow = dims.q_dtype == BS_BF16
-                         ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
-                         : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
-  if (!score_tile_finish<D, G>(n_loaded, score, qrow, dims.q_dtype, ge, tile, reduce, score_row, smem, &bar, st))
-    return;
-  if (tile >= n_tiles) return;
-  // ---- a1: the sub-block holding the appended token (tile 0, beside the others) ----
-  if (tile == 0 && tid < 32) {
+  // and the rows copied above are this CTA's.
+  const int my_tiles = (cls != BS_STREAMING && ge.c_hi > ge.c_lo) ? max(0, min(tpc, n_tiles - t0)) : 0;
+  if (my_tiles > 0) {
+    const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
+    const void *qrow = dims.q_dtype == BS_BF16
+                           ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
+                           : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
+    float *qs = reinterpret_cast<float *>(smem + L::off_q(nbuf));
+    float *dots = reinterpret_cast<float *>(smem + L::off_dots(nbuf));
+    score_load_q<D, G>(qs, qrow, dims.q_dtype);
+    for (int kk = 0; kk < my_tiles; ++kk) {
+      const int bi = kk % nbuf;
+      const int n_rows = inflight[bi];
+      if (!wait_buf(bi)) {
+        drain();
+        return;
+      }
+      score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qs, dots, ge, t0 + kk, reduce,
+                          n_rows, score_row);
+      if (kk + nbuf < my_tiles)
+        inflight[bi] = score_copy<D>(summ, tile_row(t0 + kk + nbuf), rows, smem + bi * L::kTileBytes, &bars[bi]);
+    }
+  }
+  if (!drain()) return;
+  if (cj >= n_ctas) return;
+  // ---- a1: the sub-block holding the appended token (first CTA, beside the others) --
+  if (cj == 0 && tid < 32) {
     const int j = (T - 1) / s;
     const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
     float *row = io.summaries + off + static_cast<int64_t>(j) * D;
@@ -145,9 +184,9 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
                                                         s, T, j, row);
     if (!ok && tid == 0) report(st, BS_ERR_DEVICE_BOUNDS);
   }
-  if (n_tiles > 1) {
+  if (n_ctas > 1) {
     __syncthreads();
-    if (tid == 0) is_last = (ticket_acq_rel(arrivals + u) == n_tiles - 1);
+    if (tid == 0) is_last = (ticket_acq_rel(arrivals + u) == n_ctas - 1);
     __syncthreads();
     if (!is_last) return;
   }
@@ -225,7 +264,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
     io.added_cnt[u] = nd.x;
     io.removed_cnt[u] = nd.y;
   }
-  if (tid == 0 && n_tiles > 1) arrivals[u] = 0;  // ready for the next step
+  if (tid == 0 && n_ctas > 1) arrivals[u] = 0;  // ready for the next step
 }
 
 template <int D, int G>
@@ -244,13 +283,21 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
     pt_cache = 0;
     front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, 0);
   }
-  if (front_smem < static_cast<size_t>(ScoreLayout<D, G>::kBytes)) front_smem = ScoreLayout<D, G>::kBytes;
+  // Score tiles per CTA: one while the launch fits about two waves of two CTAs per SM
+  // (short, latency-bound steps); more for large steps, up to 8, so that each CTA
+  // streams several tiles through two buffers and the grid stays near one wave.
+  const int max_tiles = dims.max_subs_per_unit / kTileRows + 2;
+  const long long work = static_cast<long long>(units) * max_tiles;
+  const int slots = attn_target_ctas();
+  const int tpc = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (work + 2 * slots - 1) / (2 * slots))));
+  const int nbuf = tpc > 1 ? 2 : 1;
+  if (front_smem < static_cast<size_t>(ScoreLayout<D, G>::bytes(nbuf))) front_smem = ScoreLayout<D, G>::bytes(nbuf);
   if (front_smem > kFrontMaxSmem) return BS_ERR_CAPACITY;
   int32_t *counters = static_cast<int32_t *>(io.workspace);
   int32_t *plist = cluster ? counters + attn_counter_floats(units) : nullptr;
-  const dim3 front_grid(units, dims.max_subs_per_unit / kTileRows + 2);
+  const dim3 front_grid(units, (max_tiles + tpc - 1) / tpc);
   if (launch_ex(step_front_kernel<D, G>, front_grid, kFrontThreads, front_smem, cs, 0, true, dims, kv, cfg, io,
-                reduce, counters, plist, pt_cache) != cudaSuccess)
+                reduce, counters, plist, pt_cache, tpc) != cudaSuccess)
     return BS_ERR_CUDA;
   AttnArgs a;
   a.dims = dims;
