@@ -106,6 +106,13 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   int inflight[2] = {0, 0}, uses[2] = {0, 0};
   for (int i = 0; i < nbuf && i < tpc; ++i)
     inflight[i] = score_copy<D>(summ, spec ? tile_row(t0 + i) : -1, rows, smem + i * L::kTileBytes, &bars[i]);
+  // The queries too: their loads fly beside the copies and the length's.
+  const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
+  const void *qrow = dims.q_dtype == BS_BF16
+                         ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
+                         : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
+  float *qs = reinterpret_cast<float *>(smem + L::off_q(nbuf));
+  if (scored) score_load_q<D, G>(qs, qrow, dims.q_dtype);
   auto wait_buf = [&](int i) -> bool {
     const bool ok = score_wait(&bars[i], static_cast<uint32_t>(uses[i] & 1), inflight[i], st);
     if (inflight[i] > 0) ++uses[i];
@@ -150,13 +157,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   // and the rows copied above are this CTA's.
   const int my_tiles = (cls != BS_STREAMING && ge.c_hi > ge.c_lo) ? max(0, min(tpc, n_tiles - t0)) : 0;
   if (my_tiles > 0) {
-    const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
-    const void *qrow = dims.q_dtype == BS_BF16
-                           ? static_cast<const void *>(static_cast<const uint16_t *>(io.q) + qbase)
-                           : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
-    float *qs = reinterpret_cast<float *>(smem + L::off_q(nbuf));
     float *dots = reinterpret_cast<float *>(smem + L::off_dots(nbuf));
-    score_load_q<D, G>(qs, qrow, dims.q_dtype);
     for (int kk = 0; kk < my_tiles; ++kk) {
       const int bi = kk % nbuf;
       const int n_rows = inflight[bi];

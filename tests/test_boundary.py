@@ -124,3 +124,42 @@ def test_calls_reject_bad_arguments_before_launch():
     # workspace too small
     assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
                                    16, st, None) == B.BS_ERR_CAPACITY
+
+
+def test_offload_and_split_calls_reject_bad_arguments():
+    """bs_block_swap, bs_cpu_sparse_attn and bs_lse_merge validate on the host first."""
+    L = B.lib()
+    ref = ctypes.byref
+    d = _dims()
+    st = 0x9000
+    cfg = B.HeadCfg(cls=0x100, block_tokens=0x200, sub_tokens=0x300, k_total=0x400, k_evict=0x500,
+                    sink_tokens=0x600, local_tokens=0x700, sum_off=0x800, sum_rows=0x900)
+    host = B.HostKV(k_pool=0x10000, v_pool=0x20000, page_table=0x30000, n_pages=128)
+    cache = B.BlockCache(k_pool=0x40000, v_pool=0x50000, page_table=0x60000, slot_block=0x70000,
+                         block_slot=0x80000, slots_per_unit=8, pages_per_slot=2)
+    swap = L.bs_block_swap
+    assert swap(ref(d), ref(cfg), 0x1000, ref(host), ref(cache), None, 0x2000, 0x3000, 0x4000, st,
+                None) == B.BS_ERR_INVALID_ARG
+    assert swap(ref(d), ref(cfg), 0x1000, ref(B.HostKV(k_pool=0, v_pool=0x20000, page_table=0x30000, n_pages=128)),
+                ref(cache), 0x1100, 0x2000, 0x3000, 0x4000, st, None) == B.BS_ERR_INVALID_ARG
+    for bad in (dict(slots_per_unit=0), dict(slots_per_unit=5000), dict(pages_per_slot=0)):
+        c = B.BlockCache(k_pool=0x40000, v_pool=0x50000, page_table=0x60000, slot_block=0x70000,
+                         block_slot=0x80000, **{**dict(slots_per_unit=8, pages_per_slot=2), **bad})
+        assert swap(ref(d), ref(cfg), 0x1000, ref(host), ref(c), 0x1100, 0x2000, 0x3000, 0x4000, st,
+                    None) == B.BS_ERR_INVALID_ARG, bad
+    misaligned = B.BlockCache(k_pool=0x40008, v_pool=0x50000, page_table=0x60000, slot_block=0x70000,
+                              block_slot=0x80000, slots_per_unit=8, pages_per_slot=2)
+    assert swap(ref(d), ref(cfg), 0x1000, ref(host), ref(misaligned), 0x1100, 0x2000, 0x3000, 0x4000, st,
+                None) == B.BS_ERR_ALIGN
+    assert swap(ref(_dims(head_dim=80)), ref(cfg), 0x1000, ref(host), ref(cache), 0x1100, 0x2000, 0x3000, 0x4000,
+                st, None) == B.BS_ERR_SHAPE
+    tables = B.HostTables(page_table=0x1000, seq_lens=0x2000, block_tokens=0x3000)
+    assert L.bs_cpu_sparse_attn(ref(d), None, ref(host), ref(tables), 0x4000, 0x5000, 0x6000, 0x7000, 4) == \
+        B.BS_ERR_INVALID_ARG
+    assert L.bs_cpu_sparse_attn(ref(d), 0x1000, ref(host), ref(B.HostTables(page_table=0, seq_lens=0x2000,
+                                                                           block_tokens=0x3000)),
+                                0x4000, 0x5000, 0x6000, 0x7000, 4) == B.BS_ERR_INVALID_ARG
+    assert L.bs_lse_merge(ref(d), 0x1000, 0x2000, None, 0x4000, 0x5000, 0x6000, None) == B.BS_ERR_INVALID_ARG
+    assert L.bs_lse_merge(ref(d), 0x1004, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == B.BS_ERR_ALIGN
+    assert L.bs_lse_merge(ref(_dims(page_size=8)), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == \
+        B.BS_ERR_SHAPE
