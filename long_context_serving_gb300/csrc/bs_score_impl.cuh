@@ -177,28 +177,4 @@ __device__ void score_compute(const float *tile_sm, const float *qs, float *dots
   __syncthreads();  // dots are free again
 }
 
-// Scores tile `tile` of a unit's candidates into row_out[c] (c = block index), one
-// buffer. summ_unit points at the unit's first summary row (16-byte aligned); qrow at
-// its G query vectors. Returns false when the bulk copy timed out. All 256 threads
-// call it with the same arguments; the tile must exist.
-template <int D, int G>
-__device__ bool score_tile(const float *summ_unit, const void *qrow, int q_dtype, const Geom &ge, int tile,
-                           int reduce, float *row_out, unsigned char *smem, uint64_t *bar, int32_t *st) {
-  using L = ScoreLayout<D, G>;
-  const int r = ge.g / ge.s;
-  const int bpt = kTileRows / r;
-  const int c_first = ge.c_lo + tile * bpt;
-  const int nb = min(bpt, ge.c_hi - c_first);
-  const int64_t row0 = static_cast<int64_t>(c_first) * r;
-  score_bars_init(bar, 1);
-  __syncthreads();
-  const int n = score_copy<D>(summ_unit, row0, row0 + nb * r, smem, bar);
-  float *qs = reinterpret_cast<float *>(smem + L::off_q(1));
-  score_load_q<D, G>(qs, qrow, q_dtype);
-  if (!score_wait(bar, 0, n, st)) return false;
-  score_compute<D, G>(reinterpret_cast<const float *>(smem), qs, reinterpret_cast<float *>(smem + L::off_dots(1)),
-                      ge, tile, reduce, n, row_out);
-  return true;
-}
-
 }  // namespace bsi

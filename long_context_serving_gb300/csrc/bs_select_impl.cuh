@@ -5,12 +5,17 @@
 // retrieval heads); "Technisches Resümee: NOSA", Methodik / 1. Algorithmus: NOSA,
 // "Dual-Selection-Mechanismus" and "ED-DMA". Set-difference: NOSA, "2. System: NOSI".
 //
-// Keys are float32 values mapped to order-preserving uint32. topk_mark finds the top k
-// with one min/max pass, one 2048-bucket histogram on (key - min) and an exact ranking
-// of the boundary bucket; topk_mark_radix (a four-pass 8-bit radix select with
-// warp-aggregated shared histograms) handles heavy ties. Ties go to the lowest block
-// index. The selection is written in ascending order by a compaction over block
-// indices, so nothing is sorted.
+// Keys are float32 values mapped to order-preserving uint32; ties go to the lowest
+// block index and every selection is written in ascending order, so nothing is sorted.
+// Two implementations of the same selection:
+//   * select_unit_regs (units with at most 32 candidates per thread, every workload
+//     here): candidates in registers, striped over the threads; top-k by refining a
+//     2048-bucket histogram level by level; output order by ballot-ranked compaction;
+//   * select_unit_flags + compact_selection (larger units): keys and flags in shared
+//     memory; top-k by one min/max pass, a 2048-bucket histogram and an exact ranking of
+//     the boundary bucket (topk_mark), with a four-pass 8-bit radix select for heavy
+//     ties (topk_mark_radix); compaction over block indices.
+// select_unit picks one. Set-difference after a selection: setdiff_sorted.
 #pragma once
 
 #include "bs_internal.cuh"
@@ -696,55 +701,6 @@ __device__ __forceinline__ int2 setdiff_sorted(const int32_t *cur, int nc, const
     if (!sorted_contains(prev, np, cur[i])) added[wa++] = cur[i];
   for (int i = pa; i < pe; ++i)
     if (!sorted_contains(cur, nc, prev[i])) removed[wr++] = prev[i];
-  const int ta = total >> 16, tr = total & 0xffff;
-  for (int i = ta + tid; i < cap; i += NT) added[i] = -1;
-  for (int i = tr + tid; i < cap; i += NT) removed[i] = -1;
-  return make_int2(ta, tr);
-}
-
-// ---------------------------------------------------------------------------
-// Set-difference of the new selection against the previous one, right after a
-// selection: membership of a previous block in the new selection is its kSel flag;
-// membership of a new block in the previous selection is a bit of `pbits` (one bit
-// per block, n_words words of shared memory). One combined scan orders both outputs.
-// cur[0, nc) and prev[0, np) are ascending lists in shared memory. All NT threads call
-// it; writes added / removed (padded with -1 to cap) and returns (added, removed).
-// ---------------------------------------------------------------------------
-template <int NT>
-__device__ __noinline__ int2 setdiff_after_select(const int32_t *cur, int nc, const int32_t *prev, int np,
-                                                  const uint8_t *flags, int n_blk, uint32_t *pbits, int n_words,
-                                                  int32_t *added, int32_t *removed, int cap, SelShared<NT> &sh) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < n_words; i += NT) pbits[i] = 0u;
-  __syncthreads();
-  for (int i = tid; i < np; i += NT) {
-    const int c = prev[i];
-    if (c >= 0 && c < n_words * 32) atomicOr(&pbits[c >> 5], 1u << (c & 31));
-  }
-  __syncthreads();
-  const int pc = (nc + NT - 1) / NT, pp = (np + NT - 1) / NT;
-  const int ca = tid * pc, ce = min(nc, ca + pc);
-  const int pa = tid * pp, pe = min(np, pa + pp);
-  int na = 0, nr = 0;
-  for (int i = ca; i < ce; ++i) {
-    const int c = cur[i];
-    na += (pbits[c >> 5] >> (c & 31)) & 1u ? 0 : 1;
-  }
-  for (int i = pa; i < pe; ++i) {
-    const int c = prev[i];
-    nr += (c >= 0 && c < n_blk && (flags[c] & kSel)) ? 0 : 1;
-  }
-  int total;
-  const int packed = block_excl_scan<NT>((na << 16) | nr, sh, &total);
-  int wa = packed >> 16, wr = packed & 0xffff;
-  for (int i = ca; i < ce; ++i) {
-    const int c = cur[i];
-    if (!((pbits[c >> 5] >> (c & 31)) & 1u)) added[wa++] = c;
-  }
-  for (int i = pa; i < pe; ++i) {
-    const int c = prev[i];
-    if (!(c >= 0 && c < n_blk && (flags[c] & kSel))) removed[wr++] = c;
-  }
   const int ta = total >> 16, tr = total & 0xffff;
   for (int i = ta + tid; i < cap; i += NT) added[i] = -1;
   for (int i = tr + tid; i < cap; i += NT) removed[i] = -1;
