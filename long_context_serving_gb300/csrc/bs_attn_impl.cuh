@@ -3,13 +3,15 @@
 // top-k selection, then sparse attention over the selected KV blocks; Kerninzichten
 // item 3: this work is bound by data movement).
 //
-// Split-KV flash-decode. A unit's selected blocks cover n_pages pages of 16 tokens;
-// they are cut into at most 32 splits of pps pages (pps a multiple of 4, chosen from
-// n_pages alone). One CTA per (split, unit):
-//   * the selection count and row are read into shared memory; warp 0 resolves
-//     page-table entries and stages pages into a ring of 4-page stages (three deep for
-//     bf16, two for fp32) with TMA copies that complete an mbarrier with their byte
-//     count;
+// Split-KV flash-decode. A unit's selected blocks cover n_pages pages of 16 tokens,
+// cut into splits of pps pages: in cluster mode (selections up to 1024 pages) S splits
+// per unit, S the largest power of two up to 16 that keeps the launch in one wave of
+// about two CTAs per SM, pps = ceil(n_pages / S); in workspace mode up to 32 splits of
+// a multiple of 4 pages. One CTA per (split, unit):
+//   * the unit's page-table row is pulled into L2 while the selection count and row are
+//     read into shared memory; warp 0 resolves the split's pages 32 at a time and stages
+//     them into a ring of 4-page stages (three deep for bf16, two for fp32) with TMA
+//     copies that complete an mbarrier with their byte count;
 //   * bf16 caches (attn_split_mma, 4 warps): each warp takes one 16-token page per
 //     stage. Pages arrive through a tiled tensor map with 128-byte swizzle, so
 //     ldmatrix reads them without bank conflicts. q.K and P.V are warp-level bf16
@@ -21,21 +23,21 @@
 //   * fp32 caches (attn_split_ffma, 8 warps): 1-D bulk copies; q.K with four threads
 //     per token over rotated 16-byte chunks, one warp per head for the softmax, and
 //     P.V with lanes owning head_dim/32 dimensions;
-//   * merge, cluster mode (selections up to 1024 pages): a unit's 16 splits are one
-//     thread-block cluster; each keeps its (o, m, l) in shared memory and, after a
-//     cluster barrier, each CTA merges a slice of the output by log-sum-exp reading
-//     its peers' shared memory (no global traffic, no atomics);
-//   * merge, workspace mode (larger selections, up to 32 splits): a unit with one
-//     split writes its output directly; otherwise each split writes an (o, m, l)
-//     record and takes an arrival ticket (one acquire-release atomic per CTA); the
-//     last split merges the records in split order.
+//   * merge, cluster mode: a unit's S splits are one thread-block cluster; each keeps
+//     its (o, m, l) in shared memory and, after a cluster barrier, each CTA merges a
+//     slice of the output by log-sum-exp reading its peers' shared memory (no global
+//     traffic, no atomics); a single split normalises its own state;
+//   * merge, workspace mode: a unit with one split writes its output directly;
+//     otherwise each split writes an (o, m, l) record and takes an arrival ticket (one
+//     acquire-release atomic per CTA); the last split merges the records in split order.
 // Tokens past T inside a partial tail page are masked out of both products.
 //
 // In step mode (the fused decode step, launched as a programmatic dependent of the
 // selection kernel) a streaming unit's blocks are its forced blocks, computed from the
 // geometry, so its splits run without waiting; every other unit waits (bounded) until
 // the selection kernel has published that unit's selection count with a release
-// store, then reads the row.
+// store, then reads its pages from the page list the selection kernel wrote (cluster
+// mode) or its row.
 #pragma once
 
 #include <cuda.h>
