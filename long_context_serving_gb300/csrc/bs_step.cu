@@ -55,7 +55,7 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 __host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel, int pt_cache_ints) {
   const size_t flags = (static_cast<size_t>(max_blocks) + 15) & ~size_t(15);
   return static_cast<size_t>(max_blocks) * 4 + flags + 2 * static_cast<size_t>(max_sel) * 4 +
-         static_cast<size_t>(pt_cache_ints) * 4;
+         (pt_cache_ints > 0 ? static_cast<size_t>(pt_cache_ints) * 4 + 32 : 0);
 }
 
 template <int D, int G>
@@ -197,20 +197,33 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   uint8_t *flags = reinterpret_cast<uint8_t *>(keys + MB);
   int32_t *cur_sm = reinterpret_cast<int32_t *>(smem + static_cast<size_t>(MB) * 4 + ((MB + 15) & ~15));
   int32_t *prev_sm = cur_sm + MS;
-  int32_t *pt_sm = prev_sm + MS;
+  int32_t *pt_sm = reinterpret_cast<int32_t *>((reinterpret_cast<uintptr_t>(prev_sm + MS) + 15) & ~uintptr_t(15));
   // The previous selection is final since the previous step: copy it asynchronously
   // (cp.async) into shared memory; it lands while the selection runs. So does the
-  // unit's page-table row when the page list is written from shared memory.
+  // unit's page-table row when the page list is written from shared memory: one bulk
+  // copy of its 16-byte-aligned span (starting up to three entries early, inside the
+  // table), the last few entries past that span read directly.
   __shared__ int np_sm;
+  __shared__ uint64_t pt_bar;
   if (tid == 0) cp_async4(&np_sm, io.prev_cnt + u);
   for (int i = tid; i < MS; i += kFrontThreads) cp_async4(prev_sm + i, io.prev_idx + srow + i);
+  cp_async_commit();
   const bool mk_plist = plist != nullptr && cls != BS_STREAMING;
   const int32_t *pt_row = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
   const int n_lp = min(dims.max_pages_per_unit, (T + kPage - 1) / kPage);
-  const bool pt_cached = mk_plist && pt_cache_ints >= n_lp;
-  if (pt_cached)
-    for (int i = tid; i < n_lp; i += kFrontThreads) cp_async4(pt_sm + i, pt_row + i);
-  cp_async_commit();
+  const uintptr_t pt_a = reinterpret_cast<uintptr_t>(pt_row);
+  const uintptr_t pt_a0 = pt_a & ~uintptr_t(15);
+  const uintptr_t pt_e0 = (pt_a + static_cast<uintptr_t>(n_lp) * 4) & ~uintptr_t(15);
+  const bool pt_cached = mk_plist && pt_cache_ints >= n_lp && pt_e0 > pt_a0;
+  const int pt_lead = static_cast<int>((pt_a - pt_a0) / 4);             // entries before the row
+  int pt_in_smem = pt_cached ? static_cast<int>((pt_e0 - pt_a) / 4) : 0;  // row entries copied
+  if (pt_cached && tid == 0) {
+    mbar_init(&pt_bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = static_cast<uint32_t>(pt_e0 - pt_a0);
+    mbar_arrive_expect_tx(&pt_bar, bytes);
+    bulk_g2s(pt_sm, reinterpret_cast<const void *>(pt_a0), bytes, &pt_bar);
+  }
   SelUnit su;
   su.cls = cls;
   su.k = k;
@@ -228,7 +241,8 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
     // Page list for the attention: the pages of the selected blocks in order (the
     // last selected block is the tail block; its pages past T are left out), -1 for
     // an entry outside the table or the pool.
-    cp_async_wait_all();
+    __syncthreads();
+    if (pt_cached && !mbar_wait_bounded(&pt_bar, 0, st)) pt_in_smem = 0;  // (reported) read global instead
     __syncthreads();
     const int ppb = g / kPage;
     const int tail_pages = min(ppb, (T - (ge.n_blk - 1) * g + kPage - 1) / kPage);
@@ -241,7 +255,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
         const int lp = c * ppb + pb;
         int phys = -1;
         if (c >= 0 && lp < n_lp && c * g + pb * kPage < T) {
-          phys = pt_cached ? pt_sm[lp] : __ldg(pt_row + lp);
+          phys = lp < pt_in_smem ? pt_sm[pt_lead + lp] : __ldg(pt_row + lp);
           if (phys < 0 || phys >= dims.n_pages) phys = -1;
         }
         pl[i] = phys;
