@@ -349,6 +349,32 @@ def measure_cpu_split(layer, wl, B, torch, reps: int = 10) -> dict:
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+_IO_OUTPUTS = ("out", "lse", "added", "added_cnt", "removed", "removed_cnt")
+
+
+def _pack_io(layers, torch, dev):
+    """Rebind every layer's q and its step outputs to views of two contiguous device
+    buffers (regions 256-byte aligned); returns (q_all, o_all)."""
+    q_all = torch.empty((len(layers),) + tuple(layers[0].q.shape), dtype=layers[0].q.dtype, device=dev)
+    for i, layer in enumerate(layers):
+        q_all[i].copy_(layer.q)
+        layer.q = q_all[i]
+    al = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    per = sum(al(getattr(layers[0], n).numel() * getattr(layers[0], n).element_size()) for n in _IO_OUTPUTS)
+    o_all = torch.zeros(len(layers) * per, dtype=torch.uint8, device=dev)
+    for i, layer in enumerate(layers):
+        off = i * per
+        for n in _IO_OUTPUTS:
+            t = getattr(layer, n)
+            nb = t.numel() * t.element_size()
+            v = o_all[off:off + nb].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            setattr(layer, n, v)
+            off += al(nb)
+    return q_all, o_all
+
+
+
 def max_over_ranks(x: float, device) -> float:
     """The largest of every rank's x (a time); x itself on a single process."""
     import torch
@@ -398,6 +424,9 @@ def run_ours(args) -> None:
     for layer in layers:
         layer.prefill()
     torch.cuda.synchronize()
+    # Every layer's queries and outputs live in two contiguous device buffers, so the
+    # end-to-end step moves its inputs and results with one copy each way.
+    q_all, o_all = _pack_io(layers, torch, dev)
 
     def layer_calls(layer):
         if args.path == "fused":
@@ -497,23 +526,19 @@ def run_ours(args) -> None:
                 "launch_us": round(per_kernel[dominant], 3),
                 "timed_as": "graph of this call over the 32 layers, us per launch"}
 
-    # End to end: every step copies q for all layers from pinned host memory, replays,
-    # and reads back out, lse and the set-difference lists into pinned host memory.
-    q_host = [torch.empty_like(l.q, device="cpu").pin_memory() for l in layers]
-    for l, h in zip(layers, q_host):
-        h.copy_(l.q.cpu())
-    outs = [(l.out, l.lse, l.added, l.added_cnt, l.removed, l.removed_cnt) for l in layers]
-    out_host = [[torch.empty_like(t, device="cpu").pin_memory() for t in o] for o in outs]
-    h2d = sum(h.numel() * h.element_size() for h in q_host)
-    d2h = sum(t.numel() * t.element_size() for o in out_host for t in o)
+    # End to end: every step copies the queries of all layers from pinned host memory
+    # (one copy), replays, and reads back out, lse and the set-difference lists of all
+    # layers into pinned host memory (one copy).
+    q_host = torch.empty_like(q_all, device="cpu").pin_memory()
+    q_host.copy_(q_all.cpu())
+    o_host = torch.empty_like(o_all, device="cpu").pin_memory()
+    h2d = q_host.numel() * q_host.element_size()
+    d2h = o_host.numel() * o_host.element_size()
 
     def e2e_step(i):
-        for l, h in zip(layers, q_host):
-            l.q.copy_(h, non_blocking=True)
+        q_all.copy_(q_host, non_blocking=True)
         graphs[i % 2].replay()
-        for o, hs in zip(outs, out_host):
-            for t, h in zip(o, hs):
-                h.copy_(t, non_blocking=True)
+        o_host.copy_(o_all, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     for i in range(args.warmup):
