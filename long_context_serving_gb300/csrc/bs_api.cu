@@ -87,7 +87,7 @@ size_t bs_workspace_size(const bs_dims *dims) {
   const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
   // Cluster mode keeps the split partials on chip: the counters and the fused step's
   // page lists. Workspace mode: the counters and the split records.
-  const size_t tail = bsi::attn_cluster_mode(dims->max_gather_pages_per_unit)
+  const size_t tail = bsi::attn_cluster_mode(static_cast<int>(units), dims->max_gather_pages_per_unit)
                           ? bsi::attn_plist_ints(units, dims->max_gather_pages_per_unit)
                           : units * bsi::kAttnMaxSplits * G * bsi::attn_record_floats(dims->head_dim);
   return (bsi::attn_counter_floats(units) + tail) * sizeof(float);

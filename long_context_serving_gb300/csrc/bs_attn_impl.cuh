@@ -176,7 +176,8 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
       ub.ok = false;
     }
   }
-  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster ? static_cast<int>(gridDim.x) : 0);
+  ub.pg = unit_pages(ub.T, ub.g, ub.ok ? ub.cnt : 0, last, in_cluster ? static_cast<int>(gridDim.x) : 0,
+                     attn_min_split_pages(dims.max_gather_pages_per_unit));
   if (ub.plist && ub.pg.n_pages > dims.max_gather_pages_per_unit) {
     if (split == 0 && tid == 0) report(st, BS_ERR_CAPACITY);
     ub.pg.n_pages = 0;

@@ -25,11 +25,25 @@ __host__ __device__ constexpr size_t attn_plist_ints(size_t units, int max_gathe
   return (units * static_cast<size_t>(max_gather) + 3) / 4 * 4;
 }
 
-// Cluster mode: a unit's splits are the 16 CTAs of one cluster and merge through
-// distributed shared memory. Workspace mode (selections above 1024 pages): up to 32
-// splits per unit merge through records in the workspace.
-__host__ __device__ inline bool attn_cluster_mode(int max_gather_pages) {
-  return max_gather_pages <= kClusterMaxPages;
+constexpr int kMidSplitPages = 32;   // workspace mode below 1024 pages: pages per split, at least
+constexpr int kClusterUnitsMax = 19; // cluster mode while units x 16 splits fit one wave of ~304 CTAs ...
+constexpr int kManyUnits = 304;      // ... or once the units alone fill it (then one split each)
+
+// Cluster mode: a unit's splits are the CTAs of one cluster and merge through
+// distributed shared memory; every unit has the same number of splits. Workspace mode:
+// selections above 1024 pages, or a middling number of units (20..303) with selections
+// that may exceed 8 x 32 pages, whose page counts can then differ a lot between units:
+// each unit's splits are sized by its own pages (at least 32 per split, so a long unit
+// gets more splits), up to 32, and merge through records in the workspace. The choice
+// depends on the dims only.
+__host__ __device__ inline bool attn_cluster_mode(int units, int max_gather_pages) {
+  if (max_gather_pages > kClusterMaxPages) return false;
+  return units <= kClusterUnitsMax || units >= kManyUnits || max_gather_pages <= 8 * kMidSplitPages;
+}
+
+// Smallest split (pages) in workspace mode.
+__host__ __device__ inline int attn_min_split_pages(int max_gather_pages) {
+  return max_gather_pages > kClusterMaxPages ? kStagePages : kMidSplitPages;
 }
 
 // Splits of a unit in cluster mode: the largest power of two (at most 16) that keeps
@@ -45,8 +59,9 @@ __host__ __device__ inline int attn_cluster_splits(int units, int max_gather_pag
 
 // Splits launched per unit.
 __host__ __device__ inline int attn_grid_splits(int units, int max_gather_pages, int slots) {
-  if (attn_cluster_mode(max_gather_pages)) return attn_cluster_splits(units, max_gather_pages, slots);
-  int splits = (max_gather_pages + kStagePages - 1) / kStagePages;
+  if (attn_cluster_mode(units, max_gather_pages)) return attn_cluster_splits(units, max_gather_pages, slots);
+  const int mn = attn_min_split_pages(max_gather_pages);
+  int splits = (max_gather_pages + mn - 1) / mn;
   if (splits > kAttnMaxSplits) splits = kAttnMaxSplits;
   return splits < 1 ? 1 : splits;
 }
@@ -61,8 +76,10 @@ struct UnitPages {
 };
 
 // The split plan depends only on the unit's own page count and the launch's splits per
-// unit in cluster mode (cluster_splits; 0 in workspace mode).
-__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk, int cluster_splits) {
+// unit in cluster mode (cluster_splits; 0 in workspace mode, where splits hold at least
+// min_pps pages).
+__device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_blk, int cluster_splits,
+                                                int min_pps) {
   UnitPages p;
   p.ppb = g / kPage;
   p.n_pages = 0;
@@ -78,6 +95,7 @@ __device__ __forceinline__ UnitPages unit_pages(int T, int g, int cnt, int last_
     int per = (p.n_pages + kStagePages * kAttnMaxSplits - 1) / (kStagePages * kAttnMaxSplits);
     if (per < 1) per = 1;
     p.pps = kStagePages * per;
+    if (p.pps < min_pps) p.pps = min_pps;
   }
   p.n_split = (p.n_pages + p.pps - 1) / p.pps;
   return p;

@@ -291,7 +291,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
   if (!attr_ok) return BS_ERR_CUDA;
   const int units = dims.batch * dims.n_kv_heads;
-  const bool cluster = attn_cluster_mode(dims.max_gather_pages_per_unit);
+  const bool cluster = attn_cluster_mode(units, dims.max_gather_pages_per_unit);
   int pt_cache = cluster && dims.max_pages_per_unit <= kPtCacheInts ? dims.max_pages_per_unit : 0;
   size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, pt_cache);
   if (front_smem > kFrontMaxSmem) {  // read the page table from global memory instead
