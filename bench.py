@@ -473,8 +473,7 @@ def run_ours(args) -> None:
 
     # Clock samples cover warm-up, the timed region and, when the timed region is
     # shorter than a second, a soak of further replays so that the sampler sees load.
-    sampler = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler = ClockSampler(local, f"{args.clocks_csv}.rank{rank}" if args.clocks_csv else None)
     for i in range(args.warmup):
         graphs[i % 2].replay()
     ms = timed_replays(graphs, args.steps)
@@ -591,6 +590,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["fused", "calls"], default="fused",
                     help="fused: bs_decode_step per layer; calls: the five separate calls per layer")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="also keep the raw nvidia-smi clock samples in this file (one per rank)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layer buffers per step (fewer only for profiling small cases)")
     ap.add_argument("--config", type=int, choices=sorted(WORKLOADS), default=CFG_ID,
