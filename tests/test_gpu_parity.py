@@ -131,6 +131,32 @@ def test_parity_shared_memory_selection_path(fused):
     rep.check()
 
 
+# GQA group sizes other than the configurations' 4 and 7 (the kernels are instantiated
+# for G = 1..8): all-retrieval (config 4 shape), dual (config 5), streaming + retrieval
+# (config 2) and the fp32 cache (config 1, head_dim 64).
+GROUPS = {
+    "cfg4-G1": (4, dict(B=2, T_range=(6000, 9000), Hq=2, Hkv=2)),
+    "cfg4-G2": (4, dict(B=2, T_range=(6000, 9000), Hq=4, Hkv=2)),
+    "cfg4-G3": (4, dict(B=2, T_range=(6000, 9000), Hq=6, Hkv=2)),
+    "cfg4-G5": (4, dict(B=2, T_range=(6000, 9000), Hq=10, Hkv=2)),
+    "cfg4-G6": (4, dict(B=2, T_range=(6000, 9000), Hq=12, Hkv=2)),
+    "cfg4-G8": (4, dict(B=2, T_range=(6000, 9000), Hq=16, Hkv=2)),
+    "cfg5-G3": (5, dict(B=1, T=2040, steps=6, Hq=6, Hkv=2)),
+    "cfg5-G8": (5, dict(B=1, T=2040, steps=6, Hq=16, Hkv=2)),
+    "cfg2-G5": (2, dict(T=4133, Hq=40, Hkv=8)),
+    "cfg1-G3": (1, dict(Hq=3, Hkv=1)),
+    "cfg1-G8": (1, dict(Hq=8, Hkv=1)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GROUPS))
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_group_sizes(name, fused):
+    cfg, kw = GROUPS[name]
+    rep = run_parity(make_workload(cfg, seed=3, **kw), fused=fused)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
