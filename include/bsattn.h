@@ -189,13 +189,22 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * and Kerninzichten item 3 (bound by data movement). For each query head h of unit
  * u, over the tokens U of the selected blocks (each clipped to t < T):
  *   out_h = sum_t softmax_t(q_h . K[t] / sqrt(d)) V[t],  lse_h = log sum_t exp(q_h . K[t] / sqrt(d)).
- * Split-KV: a unit's gathered pages are cut into contiguous splits whose size depends
- * only on that unit's page count; each split keeps an fp32 online softmax and the
- * partials are merged by log-sum-exp in split order, so the result does not depend on
- * timing. When max_gather_pages_per_unit <= 1024 a unit's 16 splits form one
- * thread-block cluster and merge through distributed shared memory; larger
- * selections use up to 32 splits whose partials go through the workspace, merged by
- * the last split to finish (an int32 arrival counter per unit).
+ * Split-KV: a unit's gathered pages are cut into contiguous splits; each split keeps an
+ * fp32 online softmax and the partials are merged by log-sum-exp in split order, so
+ * the result does not depend on timing. The plan depends on the dims and the GPU's SM
+ * count only (never on the data of other units):
+ *   - cluster mode (max_gather_pages_per_unit <= 1024, and the batch has at most 19 or
+ *     at least 304 units, or max_gather_pages_per_unit <= 256): every unit gets S
+ *     splits, S the largest power of two <= 16 with units * S <= two CTAs per SM; the
+ *     S CTAs of a unit form one thread-block cluster and merge through distributed
+ *     shared memory; split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
+ *   - workspace mode (otherwise): each unit's splits are sized by its own page count,
+ *     p = max(4 * ceil(pages / 128), m) pages per split (m = 32, or 4 when
+ *     max_gather_pages_per_unit > 1024), so at most 32 splits; partials go through the
+ *     workspace and the last split to finish merges them (an int32 arrival counter per
+ *     unit).
+ * A sub-batch launched with the same S (or in workspace mode) gives bitwise the same
+ * per-unit results as the full batch.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
  * aligned. It starts with two int32 arrival counters per unit (padded to 16 bytes);
  * these must be zero before the first call: zero the workspace once after
