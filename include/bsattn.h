@@ -225,9 +225,12 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * selections above 1024 pages per unit, split partials) lives in a fixed 8 MiB array
  * inside this library's device memory, which every GPU that loads the library keeps
  * until the process exits.
- * Limit: bs_workspace_size(dims) must not exceed 8 MiB (with selections above 1024
- * pages, head_dim 128 and G = 4 that is 62 units; below, the counters alone allow a
- * million units); larger dims return BS_ERR_CAPACITY before anything is enqueued.
+ * Limit: bs_workspace_size(dims) must not exceed 8 MiB; larger dims return
+ * BS_ERR_CAPACITY before anything is enqueued. Where the split partials go through the
+ * workspace (selections above 1024 pages, or 20 to 303 units with selections above 256
+ * pages) that is 67.6 KB per unit at head_dim 128 and G = 4: at most 124 units (62 at
+ * G = 8). In cluster mode the counters and the fused step's page lists take
+ * 8 + 4 * max_gather_pages_per_unit bytes per unit (2,044 units at 1024 pages).
  * The first call on each device looks up the array's device address with that device
  * current and caches it; make that first call before any stream capture.
  * Every call clears the arrival counters on `stream` before its kernel. All calls

@@ -48,6 +48,37 @@ def test_workspace_size():
         assert B.workspace_size(_dims(**bad)) == 0, bad
 
 
+def _ws(units, G, max_gather):
+    return B.workspace_size(_dims(batch=1, n_kv_heads=units, n_q_heads=G * units,
+                                  max_gather_pages_per_unit=max_gather))
+
+
+def test_workspace_size_modes():
+    """Two int32 counters per unit (padded to 16 bytes), then per unit either the fused
+    step's page list (cluster mode: 4 bytes per gathered page) or 32 split records of
+    G x (d + 4) floats (workspace mode), as the header states; and the 8 MiB limit of
+    the no-allocation call that follows from it."""
+    def counters(u):
+        return (2 * u + 3) // 4 * 4 * 4
+
+    def records(u, G):
+        return u * 32 * G * (128 + 4) * 4
+
+    def plist(u, mg):
+        return (u * mg + 3) // 4 * 4 * 4
+
+    assert _ws(8, 4, 1024) == counters(8) + plist(8, 1024)          # few units: cluster mode
+    assert _ws(8, 4, 2048) == counters(8) + records(8, 4)           # above 1024 pages
+    assert _ws(100, 4, 512) == counters(100) + records(100, 4)      # 20..303 units, > 256 pages
+    assert _ws(100, 4, 256) == counters(100) + plist(100, 256)
+    assert _ws(304, 4, 512) == counters(304) + plist(304, 512)      # many units: cluster mode again
+    limit = 8 << 20
+    assert _ws(124, 4, 2048) <= limit < _ws(125, 4, 2048)
+    assert _ws(62, 8, 2048) <= limit < _ws(63, 8, 2048)
+    assert _ws(124, 4, 512) <= limit < _ws(125, 4, 512) and _ws(303, 4, 512) > limit
+    assert _ws(304, 4, 1024) <= limit and _ws(2044, 4, 1024) <= limit < _ws(2045, 4, 1024)
+
+
 class HostCfg:
     """Head configuration in host memory for bs_check_head_cfg."""
 
