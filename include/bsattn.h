@@ -276,11 +276,12 @@ typedef struct {
  * appended since the last step). Only the order of fp32 additions inside the
  * attention may differ from the separate calls (streaming units split their pages
  * differently), which stays within rounding.
- * Launch 1 scores every candidate tile; tile 0 of each unit also updates a1 (that
- * sub-block lies in the forced tail block, which no score of this step reads); the
- * last tile of each unit selects, publishes the selection (cur_cnt is set to -1 first
- * and receives the count with a release store once the row is written) and writes
- * the set-difference. Launch 2 is the attention, launched as a programmatic
+ * Launch 1 scores every candidate tile (one or several 64-row tiles per CTA); the
+ * unit's first CTA also updates a1 (that sub-block lies in the forced tail block,
+ * which no score of this step reads); the unit's CTA that finishes last (an arrival
+ * ticket) selects, publishes the selection (cur_cnt is set to -1 first and receives
+ * the count with a release store once the row and the page list are written) and
+ * writes the set-difference. Launch 2 is the attention, launched as a programmatic
  * dependent: streaming units' splits start before launch 1 ends; the others wait,
  * bounded, for their unit's published count.
  * Both launches may begin before the work ahead of them in `stream` has finished;
