@@ -41,9 +41,11 @@
  *   `*dev_status` (an int32 device word the caller zeroes; atomicCAS from 0) and the
  *   offending unit's work is skipped, never performed out of bounds. Read it after
  *   synchronising.
- * Determinism. Results are bitwise reproducible run to run and independent of which
- *   other units share the batch: no floating-point atomics, and each unit's split
- *   plan depends only on that unit's own sizes.
+ * Determinism. Results are bitwise reproducible run to run (no floating-point
+ *   atomics; partials merge in a fixed order). A unit's result does not depend on the
+ *   data of the other units in the batch; it depends on their number only through the
+ *   attention's split count (bs_sparse_decode_attn), so batches launched with the same
+ *   split count give bitwise the same per-unit results.
  *
  * Data layout (dims below are the fields of bs_dims)
  * ----------------------------------------------------
