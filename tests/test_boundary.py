@@ -194,3 +194,13 @@ def test_offload_and_split_calls_reject_bad_arguments():
     assert L.bs_lse_merge(ref(d), 0x1004, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == B.BS_ERR_ALIGN
     assert L.bs_lse_merge(ref(_dims(page_size=8)), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == \
         B.BS_ERR_SHAPE
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """No fallback: without the built library every call raises."""
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "libbsattn.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        B.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        B.workspace_size(_dims())
