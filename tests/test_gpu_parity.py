@@ -157,6 +157,22 @@ def test_parity_group_sizes(name, fused):
     rep.check()
 
 
+# bf16 caches with head_dim 64 (the configurations use 128 for bf16, 64 only for fp32).
+HEAD_DIM_64 = {
+    "cfg2-d64": (2, dict(T=4133, d=64)),
+    "cfg4-d64-G7": (4, dict(B=2, T_range=(6000, 9000), d=64)),
+    "cfg5-d64-G8": (5, dict(B=1, T=2040, steps=6, Hq=16, Hkv=2, d=64)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HEAD_DIM_64))
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_bf16_head_dim_64(name, fused):
+    cfg, kw = HEAD_DIM_64[name]
+    rep = run_parity(make_workload(cfg, seed=4, **kw), fused=fused)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()

@@ -127,7 +127,7 @@ def _budget_k(frac: float, T: int, g: int) -> int:
     return max(1, int(math.floor(frac * math.ceil(T / g))))
 
 
-def _base_params(cfg_id: int, B, T, steps, Hq=None, Hkv=None):
+def _base_params(cfg_id: int, B, T, steps, Hq=None, Hkv=None, d=None):
     """Shapes and schedule of each configuration, before any random draw."""
     if cfg_id == 1:
         p = dict(name="tiny-check", B=1, Hq=4, Hkv=1, d=64, dtype="fp32", steps=1, T_first=2048,
@@ -157,6 +157,8 @@ def _base_params(cfg_id: int, B, T, steps, Hq=None, Hkv=None):
         p["Hq"] = Hq
     if Hkv is not None:
         p["Hkv"] = Hkv
+    if d is not None:
+        p["d"] = d
     if p["Hq"] % p["Hkv"] != 0:
         raise ValueError("Hq must be a multiple of Hkv")
     return p
@@ -164,16 +166,16 @@ def _base_params(cfg_id: int, B, T, steps, Hq=None, Hkv=None):
 
 def make_workload(cfg_id: int, seed: int = 0, *, B: int | None = None, T: int | None = None,
                   steps: int | None = None, T_range: tuple | None = None, Hq: int | None = None,
-                  Hkv: int | None = None) -> Workload:
+                  Hkv: int | None = None, d: int | None = None) -> Workload:
     """Build configuration ``cfg_id`` (1..5) from ``seed``.
 
     Overrides shrink a configuration for tests: ``B`` sequences, ``T`` tokens in the
     cache at the first decode step (all sequences), ``T_range`` = (lo, hi) for the
     per-sequence length draw of configuration 4, ``steps`` decode steps, ``Hq`` and
     ``Hkv`` the query and KV head counts (other GQA group sizes; configuration 2 makes
-    its KV heads 0-3 streaming and the rest retrieval).
+    its KV heads 0-3 streaming and the rest retrieval), ``d`` the head dimension.
     """
-    p = _base_params(cfg_id, B, T, steps, Hq, Hkv)
+    p = _base_params(cfg_id, B, T, steps, Hq, Hkv, d)
     if T_range is not None:
         p["T_lo"], p["T_hi"] = T_range
     Bn, Hq, Hkv, d, steps_n = p["B"], p["Hq"], p["Hkv"], p["d"], p["steps"]
