@@ -34,9 +34,10 @@ class PagedLayer:
     reading past T would show up (NaN by default).
     ``preload_all``: put every token of every step in the pool now (otherwise tokens
     enter the pool when their step appends them).
+    ``q_fp32``: pass the queries as fp32 (the same values, widened) over a bf16 cache.
     """
 
-    def __init__(self, wl, device="cuda", fill=float("nan"), preload_all=False):
+    def __init__(self, wl, device="cuda", fill=float("nan"), preload_all=False, q_fp32=False):
         self.wl = wl
         self.device = torch.device(device)
         U, d, G = wl.U, wl.d, wl.G
@@ -56,7 +57,7 @@ class PagedLayer:
                            max_sel_per_unit=self.max_sel, max_subs_per_unit=int(sub_rows.max()),
                            max_gather_pages_per_unit=int((sel_u * g // 16).max()), n_pages=int(wl.n_pages),
                            kv_dtype=B.BS_BF16 if wl.dtype == "bf16" else B.BS_FP32,
-                           q_dtype=B.BS_BF16 if wl.dtype == "bf16" else B.BS_FP32)
+                           q_dtype=B.BS_BF16 if wl.dtype == "bf16" and not q_fp32 else B.BS_FP32)
 
         dev = self.device
         i32 = lambda a: torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32), device=dev)  # noqa: E731
@@ -89,6 +90,8 @@ class PagedLayer:
         self._write_tokens(np.zeros(wl.B, np.int64), upto)
 
         self.q = _kv_tensor(wl.q, wl.dtype, dev)           # [steps][B][Hq][d]
+        if q_fp32:
+            self.q = self.q.float().contiguous()
         self.seq_lens = i32(np.stack([wl.T_prefill + i + 1 for i in range(wl.steps)]))  # [steps][B]
         self.tok_begin = self.seq_lens - 1
         self.prefill_lens = i32(wl.T_prefill)

@@ -58,9 +58,10 @@ def attention_errors(o_gpu: np.ndarray, o_ref: np.ndarray):
 
 
 def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_sample=None, seed=0,
-               fused=False) -> Report:
+               fused=False, q_fp32=False) -> Report:
     """Drive the GPU path and the oracle through the same steps on ``units`` (default all).
 
+    ``q_fp32``: queries passed as fp32 (the same values) over the bf16 cache.
     ``fused``: run each step through bs_decode_step (one call for all five steps). A
     near-tie unit whose GPU selection differs from the oracle's then cannot be given
     the oracle's selection before attention: its attention and set-difference are not
@@ -69,7 +70,7 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
     units = list(range(wl.U)) if units is None else list(units)
     reduce_code = B.BS_GROUP_MAX if group_reduce == "max" else B.BS_GROUP_MEAN
     rng = np.random.default_rng(seed)
-    layer = PagedLayer(wl)
+    layer = PagedLayer(wl, q_fp32=q_fp32)
     layer.prefill()
     state = O.init_state(wl, units)
     rep = Report()

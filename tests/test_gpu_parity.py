@@ -173,6 +173,23 @@ def test_parity_bf16_head_dim_64(name, fused):
     rep.check()
 
 
+@pytest.mark.parametrize("kw", [dict(d=128), dict(d=128, Hq=8, Hkv=1)], ids=["G4", "G8"])
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_fp32_head_dim_128(kw, fused):
+    """fp32 caches at head_dim 128 (configuration 1 uses 64)."""
+    rep = run_parity(make_workload(1, seed=6, **kw), fused=fused)
+    rep.check()
+
+
+@pytest.mark.parametrize("name", ["cfg2-T4133", "cfg5-B4-T2040x16"])
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_fp32_queries_over_bf16_cache(name, fused):
+    """q_dtype fp32 with a bf16 cache: the same query values, widened."""
+    cfg, kw = SMALL[name]
+    rep = run_parity(make_workload(cfg, seed=7, **kw), fused=fused, q_fp32=True)
+    rep.check()
+
+
 def test_parity_group_mean():
     rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
     rep.check()
