@@ -190,8 +190,9 @@ def test_parity_fp32_queries_over_bf16_cache(name, fused):
     rep.check()
 
 
-def test_parity_group_mean():
-    rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean")
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_group_mean(fused):
+    rep = run_parity(make_workload(2, seed=2, T=3000), group_reduce="mean", fused=fused)
     rep.check()
 
 
