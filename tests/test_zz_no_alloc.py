@@ -35,8 +35,13 @@ def _close(a, ref):
     assert float((diff / ref.double().abs().clamp_min(REL_FLOOR)).max()) <= ATT_REL
 
 
-def test_noalloc_matches_workspace_entry_point_on_two_calls():
-    wl = make_workload(2, seed=11, T=5000)
+@pytest.mark.parametrize("large", [False, True], ids=["cluster-merge", "scratch-merge"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(large):
+    """Small selections merge their splits on chip; selections above 1024 pages keep
+    their split partials in the fixed scratch array."""
+    wl = make_workload(2, seed=11, T=20000 if large else 5000)
+    if large:
+        wl.k[4:] = 600                  # ~1200 pages per retrieval unit
     layer = PagedLayer(wl)
     layer.prefill()
     layer.append(0)
