@@ -6,7 +6,6 @@ tokens into the paged pool; every step of the decode path is a libbsattn call.
 from __future__ import annotations
 
 import ctypes
-import math
 
 import numpy as np
 import torch

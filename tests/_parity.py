@@ -15,7 +15,6 @@ GPU attention and set-difference so that both sides keep the same state.
 """
 from __future__ import annotations
 
-import math
 from dataclasses import dataclass, field
 
 import numpy as np

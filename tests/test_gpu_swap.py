@@ -5,7 +5,6 @@ every block, block of every slot, cache page table) equals the oracle's exactly,
 cached pages equal the host pool's bytes, and attention over the cache equals
 attention over the full pool (bitwise for the separate calls: same values, same split
 plan)."""
-import ctypes
 
 import numpy as np
 import pytest

@@ -7,7 +7,6 @@ bs_sparse_decode_attn with a caller-allocated workspace, and that a shape too la
 for its fixed scratch array is refused on the host. It lives in a file of its own so
 that pytest collects it last.
 """
-import numpy as np
 import pytest
 import torch
 
