@@ -132,6 +132,39 @@ def _swap_highest_slot_first(slot_block, block_slot, added, removed):
     return sb, bs, copies
 
 
+def _decode_step_variant(drop: str):
+    """decode_step with one piece of its carried state left out: 'alive' (the eviction
+    mask is not carried), 'prev_sel' (the previous selection is not recorded) or 'kbar'
+    (the updated summaries are not stored back)."""
+    def step(wl, step_i, state, units=None, group_reduce="max"):
+        units = range(wl.U) if units is None else units
+        out = {}
+        for u in units:
+            st = state[u]
+            b = wl.unit_seq(u)
+            T = wl.T(step_i, b)
+            g, s = int(wl.g[u]), int(wl.s[u])
+            K = wl.K64(u)
+            kbar = O.update_sub_block(st.kbar if drop != "kbar" else st.kbar.copy(), K, T, s)
+            if drop != "kbar":
+                st.kbar = kbar
+            q = wl.q64(step_i, u)
+            cls = int(wl.cls[u])
+            scores = O.block_scores(q, kbar, T, g, s, group_reduce) if cls != O.STREAMING else None
+            evict = wl.evict[u] if cls == O.DUAL else None
+            sel = O.select_unit(cls, T, g, int(wl.sink[u]), int(wl.local[u]), int(wl.k[u]), int(wl.k_e[u]),
+                                scores, evict, st.alive)
+            if cls == O.DUAL and drop != "alive":
+                st.alive = sel.alive
+            o, lse = O.sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
+            added, removed = O.setdiff(st.prev_sel, sel.sel)
+            if drop != "prev_sel":
+                st.prev_sel = list(sel.sel)
+            out[u] = O.UnitStep(T=T, sel=sel, scores=scores, o=o, lse=lse, added=added, removed=removed)
+        return out
+    return step
+
+
 MUTATIONS = {
     "means_divide_by_s": ("sub_block_means", _means_divide_by_s),
     "scores_no_scale": ("block_scores", _scores_no_scale),
@@ -152,6 +185,9 @@ MUTATIONS = {
     "update_wrong_sub_block": ("update_sub_block", _update_wrong_sub_block),
     "swap_no_free": ("block_swap", _swap_no_free),
     "swap_highest_slot_first": ("block_swap", _swap_highest_slot_first),
+    "decode_step_alive_not_carried": ("decode_step", _decode_step_variant("alive")),
+    "decode_step_prev_sel_not_carried": ("decode_step", _decode_step_variant("prev_sel")),
+    "decode_step_kbar_not_stored": ("decode_step", _decode_step_variant("kbar")),
 }
 
 ORIG = {name: getattr(O, name) for name, _ in MUTATIONS.values()}
@@ -167,4 +203,22 @@ def test_planted_mistake_is_caught(mutation, monkeypatch):
             check(O)
         except Exception as e:  # noqa: BLE001 - any failure of a pin counts
             failed.append((check.__name__, type(e).__name__))
+            break                # one failing pin is enough
     assert failed, f"no pin caught the planted mistake {mutation}"
+
+
+def test_decode_step_variant_is_faithful_when_nothing_is_dropped():
+    """The decode_step copy the carry mutations start from equals the oracle's own when
+    nothing is dropped, so each of those mutations differs from the oracle by its one
+    left-out assignment only."""
+    from workloads import make_workload
+    wl = make_workload(5, seed=3, B=1, T=2040, steps=10)
+    a, b = O.init_state(wl), O.init_state(wl)
+    same = _decode_step_variant("")
+    for step in range(wl.steps):
+        ra, rb = O.decode_step(wl, step, a), same(wl, step, b)
+        for u in range(wl.U):
+            assert ra[u].sel.sel == rb[u].sel.sel and ra[u].added == rb[u].added
+            assert ra[u].removed == rb[u].removed
+            np.testing.assert_array_equal(ra[u].o, rb[u].o)
+            np.testing.assert_array_equal(a[u].alive, b[u].alive)

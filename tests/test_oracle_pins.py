@@ -390,11 +390,84 @@ def check_p11_block_swap_invariants(orc):
             prev = sel
 
 
+# ---------------------------------------------------------------------------
+# P12: the state decode_step carries from one step to the next
+# ---------------------------------------------------------------------------
+def _plain_means(K, T, s):
+    """Sub-block means by cumulative sums (a different route from a per-block mean)."""
+    cs = np.concatenate([np.zeros((1, K.shape[1])), np.cumsum(np.asarray(K[:T], np.float64), axis=0)])
+    lo = np.arange(0, T, s)
+    hi = np.minimum(lo + s, T)
+    return (cs[hi] - cs[lo]) / (hi - lo)[:, None]
+
+
+def check_p12_decode_step_carry(orc):
+    """Multi-step runs through init_state + decode_step on a dual workload that crosses
+    a block boundary and on a mixed streaming/retrieval workload whose units have
+    different block sizes. At every step the carried state must follow the rules the
+    pages fix ("Technisches Resümee: NOSA", Dual-Selection-Mechanismus: a block that
+    left Gamma_e's pool never returns to it; Lokalitätsgarantie: at least k_e of the
+    k selected blocks were selected at the previous step): the summaries equal a rebuild
+    at the current length, the set-difference is the one between this step's and the
+    previous step's selections, and the carried alive mask marks exactly the blocks never
+    dropped from Gamma_e's pool."""
+    cases = [make_workload(5, seed=3, B=2, T=2040, steps=14),      # crosses T = 2048 (g = 64)
+             make_workload(3, seed=5, B=1, T=4090, steps=12)]      # crosses T = 4096 for every g
+    assert {int(c) for c in cases[1].cls} == {orc.STREAMING, orc.RETRIEVAL}
+    assert len({int(x) for x in cases[1].g}) > 1
+    for wl in cases:
+        state = orc.init_state(wl)
+        prev_sel = {u: [] for u in range(wl.U)}
+        prev_e = {u: None for u in range(wl.U)}
+        prev_C = {u: None for u in range(wl.U)}
+        dropped = {u: set() for u in range(wl.U)}
+        crossed = False
+        for step in range(wl.steps):
+            res = orc.decode_step(wl, step, state)
+            for u in range(wl.U):
+                r, st = res[u], state[u]
+                b = wl.unit_seq(u)
+                T = wl.T(step, b)
+                assert r.T == T
+                g, s, k_e = int(wl.g[u]), int(wl.s[u]), int(wl.k_e[u])
+                # summaries carried = rebuilt at this length
+                n_sub = -(-T // s)
+                assert st.kbar.shape[0] >= n_sub
+                np.testing.assert_allclose(st.kbar[:n_sub], _plain_means(wl.K64(u), T, s), rtol=0, atol=1e-9)
+                # set-difference against the previous step's selection
+                cur = np.array(r.sel.sel, dtype=np.int64)
+                prv = np.array(prev_sel[u], dtype=np.int64)
+                assert r.added == np.setdiff1d(cur, prv).tolist(), (step, u)
+                assert r.removed == np.setdiff1d(prv, cur).tolist(), (step, u)
+                C = {c for c in range(T // g)
+                     if not (c < -(-int(wl.sink[u]) // g) or c >= max(0, T - int(wl.local[u])) // g)}
+                if wl.cls[u] == orc.DUAL:
+                    E = set(r.sel.gamma_e)
+                    assert len(E) <= k_e and E <= C
+                    assert not (E & dropped[u]), (step, u)                         # P4
+                    if prev_e[u] is not None:
+                        C_new = C - prev_C[u]
+                        crossed |= bool(C_new)
+                        assert E <= prev_e[u] | C_new, (step, u)                   # P4
+                        if len(E) == k_e:
+                            assert len((E | set(r.sel.gamma_q)) & set(prev_sel[u])) >= k_e, (step, u)  # P5
+                    dropped[u] |= C - E
+                    n_cap = st.alive.shape[0]
+                    want = np.ones(n_cap, np.uint8)
+                    want[sorted(dropped[u])] = 0
+                    np.testing.assert_array_equal(st.alive, want, err_msg=f"alive, step {step} unit {u}")
+                    prev_e[u] = E
+                prev_C[u] = C
+                prev_sel[u] = list(r.sel.sel)
+        if (wl.cls == orc.DUAL).any():
+            assert crossed, "the dual run must bring new candidates in"
+
+
 ALL_CHECKS = [check_golden_pooling, check_golden_select_retrieval, check_golden_select_dual,
               check_golden_attention, check_p1_full_budget_is_dense, check_p2_streaming_is_sink_window,
               check_p3_select_brute_force, check_p4_p5_eviction, check_p6_pooling_special_cases,
               check_p7_setdiff, check_p8_planted, check_p9_lse_merge, check_p10_incremental,
-              check_golden_block_swap, check_p11_block_swap_invariants]
+              check_golden_block_swap, check_p11_block_swap_invariants, check_p12_decode_step_carry]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
