@@ -100,7 +100,9 @@ typedef enum { BS_STREAMING = 0, BS_RETRIEVAL = 1, BS_DUAL = 2 } bs_head_class;
 typedef enum { BS_GROUP_MAX = 0, BS_GROUP_MEAN = 1 } bs_group_reduce;
 
 /* Shapes and capacities, host struct. Supported: head_dim 64 or 128, page_size 16,
- * G = n_q_heads / n_kv_heads in 1..8, max_blocks_per_unit <= 16384. */
+ * G = n_q_heads / n_kv_heads in 1..8, max_blocks_per_unit <= 16384, and pools of at
+ * most (2^31 - 1) / 16 pages (pool rows are signed 32-bit tensor-map coordinates);
+ * larger values return BS_ERR_CAPACITY. */
 typedef struct {
   int32_t batch, n_q_heads, n_kv_heads, head_dim, page_size;
   int32_t max_pages_per_unit;        /* page-table row length */
@@ -234,7 +236,10 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * G = 8). In cluster mode the counters and the fused step's page lists take
  * 8 + 4 * max_gather_pages_per_unit bytes per unit (2,044 units at 1024 pages).
  * The first call on each device looks up the array's device address with that device
- * current and caches it; make that first call before any stream capture.
+ * current and caches it; make that first call before any stream capture. The cached
+ * address belongs to the device's context at that time: after cudaDeviceReset (or
+ * anything else that destroys and re-creates the device's primary context) it is stale,
+ * so do not call this entry point again in that process.
  * Every call clears the arrival counters on `stream` before its kernel. All calls
  * share the one array per device, so calls whose kernels overlap on the GPU (on
  * different streams, or from different threads) race and corrupt each other's

@@ -1,5 +1,6 @@
 // Host-side parts of the C ABI that launch nothing: status text, shape checks,
 // head-configuration checks and workspace sizing.
+#include <climits>
 #include <cstdint>
 
 #include "bs_attn_plan.cuh"
@@ -21,6 +22,9 @@ bs_status check_dims(const bs_dims *d) {
       d->max_subs_per_unit < 1 || d->max_gather_pages_per_unit < 1 || d->n_pages < 1)
     return BS_ERR_INVALID_ARG;
   if (d->max_blocks_per_unit > kMaxBlocks) return BS_ERR_CAPACITY;
+  // The attention's tensor maps address pool rows (16 per page) with signed 32-bit
+  // coordinates: every row must stay below 2^31.
+  if (d->n_pages > static_cast<int64_t>(INT32_MAX) / kPage) return BS_ERR_CAPACITY;
   if (static_cast<int64_t>(d->batch) * d->n_kv_heads > (int64_t(1) << 24)) return BS_ERR_CAPACITY;
   return BS_OK;
 }
@@ -48,7 +52,7 @@ bs_status make_kv_tensor_maps(const bs_dims &d, const bs_kv &kv, CUtensorMap *tk
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return BS_ERR_CUDA;
   const uint64_t rows = static_cast<uint64_t>(d.n_pages) * kPage;
-  if (rows > (uint64_t(1) << 32)) return BS_ERR_CAPACITY;
+  if (rows > static_cast<uint64_t>(INT32_MAX)) return BS_ERR_CAPACITY;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d.head_dim), rows};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d.head_dim) * 2};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};

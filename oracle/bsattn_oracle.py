@@ -306,8 +306,8 @@ class UnitStep:
     T: int
     sel: Selection
     scores: np.ndarray | None
-    o: np.ndarray
-    lse: np.ndarray
+    o: np.ndarray | None
+    lse: np.ndarray | None
     added: list
     removed: list
 
@@ -328,8 +328,12 @@ def init_state(wl, units=None) -> dict:
     return state
 
 
-def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max") -> dict:
-    """Run one decode step for ``units`` (default: all); update ``state`` in place."""
+def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max", attend_units=None) -> dict:
+    """Run one decode step for ``units`` (default: all); update ``state`` in place.
+
+    ``attend_units``: when given, the attention output (o, lse) is computed only for
+    these units and is None for the others; every other result is computed for all
+    ``units``."""
     units = range(wl.U) if units is None else units
     out = {}
     for u in units:
@@ -349,7 +353,9 @@ def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max
                           int(wl.k_e[u]), scores, evict, st.alive)
         if cls == DUAL:
             st.alive = sel.alive
-        o, lse = sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
+        o = lse = None
+        if attend_units is None or u in attend_units:
+            o, lse = sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
         added, removed = setdiff(st.prev_sel, sel.sel)
         st.prev_sel = list(sel.sel)
         out[u] = UnitStep(T=T, sel=sel, scores=scores, o=o, lse=lse, added=added, removed=removed)

@@ -48,6 +48,24 @@ def test_workspace_size():
         assert B.workspace_size(_dims(**bad)) == 0, bad
 
 
+def test_pool_rows_stay_below_two_to_the_31():
+    """Pool rows (16 per page) are signed 32-bit tensor-map coordinates: a pool of 2^27
+    pages (2^31 rows) is refused on the host by every call, one page fewer is accepted."""
+    assert B.workspace_size(_dims(n_pages=(1 << 27) - 1)) > 0
+    big = _dims(n_pages=1 << 27)
+    assert B.workspace_size(big) == 0
+    L = B.lib()
+    kv = B.KV(k_pool=0x10000, v_pool=0x20000, page_table=0x30000, seq_lens=0x40000)
+    cfg = B.HeadCfg(*([0x50000] * 9))
+    ref = ctypes.byref
+    assert L.bs_sparse_decode_attn(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+                                   1 << 30, 0x6000, None) == B.BS_ERR_CAPACITY
+    assert L.bs_sparse_decode_attn_noalloc(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000,
+                                           0x6000, None) == B.BS_ERR_CAPACITY
+    assert L.bs_build_block_summaries(ref(big), ref(kv), ref(cfg), 0x1000, 1, 0x70000, 0x6000, None) == \
+        B.BS_ERR_CAPACITY
+
+
 def _ws(units, G, max_gather):
     return B.workspace_size(_dims(batch=1, n_kv_heads=units, n_q_heads=G * units,
                                   max_gather_pages_per_unit=max_gather))

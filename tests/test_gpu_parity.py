@@ -1,4 +1,6 @@
 """GPU parity of the five calls against the float64 oracle (through the C ABI)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -43,14 +45,6 @@ def test_parity_small(name):
 def test_parity_small_fused_step(name):
     cfg, kw = SMALL[name]
     rep = run_parity(make_workload(cfg, seed=1, **kw), fused=True)
-    rep.check()
-
-
-@pytest.mark.parametrize("cfg,n_units", [(2, None), (3, 6), (4, 6), (5, 6)])
-def test_parity_full_size_fused_step(cfg, n_units):
-    wl = make_workload(cfg, seed=0)
-    units = None if n_units is None else _sample_units(wl, n_units)
-    rep = run_parity(wl, units, summary_rows_sample=None if cfg <= 2 else 256, fused=True)
     rep.check()
 
 
@@ -207,11 +201,22 @@ def _sample_units(wl, n):
     return sorted(set(pick))[:max(n, 2)]
 
 
-@pytest.mark.parametrize("cfg,n_units", [(1, None), (2, None), (3, 6), (4, 6), (5, 6)])
-def test_parity_full_size(cfg, n_units):
-    wl = make_workload(cfg, seed=0)
-    units = None if n_units is None else _sample_units(wl, n_units)
-    rep = run_parity(wl, units, summary_rows_sample=None if cfg <= 2 else 256)
+@functools.lru_cache(maxsize=1)
+def _full_workload(cfg):
+    return make_workload(cfg, seed=0)
+
+
+@pytest.mark.parametrize("cfg,fused", [(1, False), (2, False), (2, True), (3, False), (3, True), (4, False),
+                                       (4, True), (5, False), (5, True)])
+def test_parity_full_size(cfg, fused):
+    """Full-size configurations through the five calls and through the fused step:
+    summaries (256 sampled rows per unit from config 3 on), scores, selections, alive
+    masks and set-differences of every unit at every step; the attention output of every
+    unit for configs 1 and 2 and of six sampled units (both classes) for configs 3-5."""
+    wl = _full_workload(cfg)
+    attend = None if cfg <= 2 else set(_sample_units(wl, 6))
+    rep = run_parity(wl, None, summary_rows_sample=None if cfg <= 2 else 256, fused=fused, attend_units=attend)
+    assert rep.selection_checks == wl.U * wl.steps
     rep.check()
 
 

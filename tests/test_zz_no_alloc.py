@@ -3,16 +3,19 @@
 It serves callers that cannot allocate device memory, such as a plugin whose host
 engine owns all allocations, or a serving loop that must not call cudaMalloc after
 start-up. The test drives it through the C ABI and checks two calls in a row against
-bs_sparse_decode_attn with a caller-allocated workspace, and that a shape too large
-for its fixed scratch array is refused on the host. It lives in a file of its own so
-that pytest collects it last.
+bs_sparse_decode_attn with a caller-allocated workspace and against the float64
+oracle's attention over the same selections, and that a shape too large for its fixed
+scratch array is refused on the host. It lives in a file of its own so that pytest
+collects it last.
 """
+import numpy as np
 import pytest
 import torch
 
 from long_context_serving_gb300 import bsattn as B
 from long_context_serving_gb300.build import build
 from long_context_serving_gb300.layer import PagedLayer
+from oracle import bsattn_oracle as O
 from workloads import make_workload
 
 pytestmark = pytest.mark.gpu
@@ -51,6 +54,15 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(large):
     torch.cuda.synchronize()
     ref_out, ref_lse = layer.out.clone(), layer.lse.clone()
     assert layer.read_status() == 0
+    # The float64 oracle's attention over the selections the GPU made.
+    sel = layer.selection(layer.cur)
+    oracle_out = np.zeros(tuple(layer.out.shape))
+    oracle_lse = np.zeros(tuple(layer.lse.shape))
+    for u in range(wl.U):
+        b, hk = divmod(u, wl.Hkv)
+        o, lse = O.sparse_attention(wl.q64(0, u), wl.K64(u), wl.V64(u), sel[u], int(wl.g[u]), wl.T(0, b))
+        oracle_out[b, hk * wl.G:(hk + 1) * wl.G] = o
+        oracle_lse[b, hk * wl.G:(hk + 1) * wl.G] = lse
     for _ in range(2):
         layer.out.fill_(float("nan"))
         layer.lse.fill_(float("nan"))
@@ -61,6 +73,8 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(large):
         assert layer.read_status() == 0
         _close(layer.out, ref_out)
         _close(layer.lse, ref_lse)
+        _close(layer.out, torch.from_numpy(oracle_out).to(layer.out.device))
+        assert float((layer.lse.double().cpu() - torch.from_numpy(oracle_lse)).abs().max()) <= ATT_ABS
 
 
 def test_noalloc_refuses_dims_beyond_its_scratch():
