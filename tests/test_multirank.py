@@ -53,7 +53,7 @@ def test_ranks_serve_distinct_batches():
 
 def test_reference_arm_prints_on_rank0_only(monkeypatch, capsys):
     class Args:
-        steps, warmup, gpus = 1, 3, 2
+        steps, warmup, gpus, config = 1, 3, 2, bench.DEFAULT_CFG
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
@@ -63,12 +63,25 @@ def test_reference_arm_prints_on_rank0_only(monkeypatch, capsys):
 def test_reference_arm_line(monkeypatch, capsys, world):
     """Rank 0's reference line carries the contract's keys (oracle timed on a tiny sample)."""
     monkeypatch.setenv("RANK", "0")
-    monkeypatch.setattr(bench, "time_oracle", lambda reps, warm: {
-        "value": 123.0, "unit": bench.UNIT, "cores": 1, "kind": "oracle", "sample": "stub", "times_s": []})
+    monkeypatch.setattr(bench, "time_oracle", lambda cfg, reps, warm, **kw: {
+        "value": 123.0, "unit": bench.UNIT, "cores": 4, "kind": "oracle", "sample": "stub",
+        "mean_step_ms": 0.125})
 
     class Args:
-        steps, warmup, gpus = 2, 3, world
+        steps, warmup, gpus, config = 2, 3, world, bench.DEFAULT_CFG
     bench.run_reference(Args())
     line = json.loads(capsys.readouterr().out.strip())
     assert line["impl"] == "reference" and line["n_gpus"] == world and line["higher_is_better"] is False
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+    # ms_per_step is the time of one timed step (one layer), not a multiple of it
+    assert line["ms_per_step"] == 0.125 and line["config"]["layers_per_step"] == 1
+    assert line["cpu_baseline"]["cores"] == 4
+
+
+def test_oracle_timing_runs_on_several_processes():
+    """The CPU baseline's oracle timing forks worker processes over the units of one
+    layer (tiny configuration) and reports the process count and a one-process figure."""
+    res = bench.time_oracle(1, reps=2, warm=1, single_reps=1, workers=2)
+    assert res["kind"] == "oracle" and res["value"] > 0 and res["unit"] == bench.UNIT
+    assert res["cores"] == 1                    # the tiny configuration has one unit
+    assert res["single_thread"]["cores"] == 1 and res["single_thread"]["value"] > 0
