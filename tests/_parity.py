@@ -30,10 +30,13 @@ SUM_ABS = 1e-4
 SCORE_ABS, SCORE_REL = 3e-4, 1e-5
 
 
-# Near-ties may exclude at most this share of the compared selections (at least one):
-# a kernel that produced near-tie-looking scores everywhere cannot pass by having its
-# selections replaced with the oracle's.
-NEAR_TIE_SHARE = 0.05
+# Near-ties may make up at most this share of the compared selections (at least one).
+# With thousands of candidates a unit's k-th and (k+1)-th scores often lie within the
+# near-tie band (up to about one retrieval unit-step in six at 8,193 candidates), so
+# this cap is loose; what keeps a near-tie from hiding a wrong selection is the exact
+# check below: every selection the GPU makes, near-tie or not, must be the selection
+# rule applied to the GPU's own fp32 scores, and those scores must match the oracle's.
+NEAR_TIE_SHARE = 0.25
 
 
 @dataclass
@@ -104,6 +107,7 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
             layer.select(step)
             sel_buf = layer.cur
         torch.cuda.synchronize()
+        alive_before = {u: None if state[u].alive is None else state[u].alive.copy() for u in units}
         res = O.decode_step(wl, step, state, units, group_reduce, attend_units=attend_units)
         gsel = layer.selection(sel_buf)
         scores = layer.scores.cpu().numpy()
@@ -128,7 +132,18 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
                     mask = np.ones(layer.max_blocks, bool)
                     mask[C] = False
                     assert np.all(scores[u, mask] == -np.inf), (step, u)
-            # a3: selection
+            # a3: the selection kernel is exact on its own inputs: the oracle's rule applied
+            # to the GPU's fp32 scores (and the same eviction logits and alive mask) gives
+            # the GPU's selection, at every unit, near-tie or not.
+            if wl.cls[u] != O.STREAMING:
+                ev = None
+                if wl.cls[u] == O.DUAL:
+                    ev = np.full(layer.max_blocks, -np.inf)
+                    n_ev = min(layer.max_blocks, wl.evict.shape[1])
+                    ev[:n_ev] = wl.evict[u, :n_ev]
+                own = O.select_unit(int(wl.cls[u]), r.T, g, int(wl.sink[u]), int(wl.local[u]), int(wl.k[u]),
+                                    int(wl.k_e[u]), scores[u].astype(np.float64), ev, alive_before[u])
+                assert gsel[u] == own.sel, (step, u, "selection differs from the rule on the GPU's own scores")
             rep.selection_checks += 1
             if r.sel.near_tie:
                 rep.near_ties += 1
