@@ -489,7 +489,8 @@ class Bench:
             for layer in self.layers:
                 self.layer_calls(layer, i % self.wl.steps)
         torch.cuda.synchronize()
-        assert all(layer.read_status() == 0 for layer in self.layers), "device status set during warm-up"
+        codes = [layer.read_status() for layer in self.layers]
+        assert not any(codes), f"device status set during warm-up: {codes}"
         self.cap = torch.cuda.Stream(device=dev)
         self.graphs = []
         for i in range(self.n_graph):

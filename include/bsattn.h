@@ -42,10 +42,9 @@
  *   offending unit's work is skipped, never performed out of bounds. Read it after
  *   synchronising.
  * Determinism. Results are bitwise reproducible run to run (no floating-point
- *   atomics; partials merge in a fixed order). A unit's result does not depend on the
- *   data of the other units in the batch; it depends on their number only through the
- *   attention's split count (bs_sparse_decode_attn), so batches launched with the same
- *   split count give bitwise the same per-unit results.
+ *   atomics; partials merge in a fixed order). Selections never depend on the other
+ *   units of the batch; attention outputs depend on them only through the attention's
+ *   plan (bs_sparse_decode_attn), in the last bits.
  *
  * Data layout (dims below are the fields of bs_dims)
  * ----------------------------------------------------
@@ -193,27 +192,38 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * and Kerninzichten item 3 (bound by data movement). For each query head h of unit
  * u, over the tokens U of the selected blocks (each clipped to t < T):
  *   out_h = sum_t softmax_t(q_h . K[t] / sqrt(d)) V[t],  lse_h = log sum_t exp(q_h . K[t] / sqrt(d)).
- * Split-KV: a unit's gathered pages are cut into contiguous splits; each split keeps an
- * fp32 online softmax and the partials are merged by log-sum-exp in split order, so
- * the result does not depend on timing. The plan depends on the dims and the GPU's SM
- * count only (never on the data of other units):
- *   - cluster mode (max_gather_pages_per_unit <= 1024, and the batch has at most 19 or
- *     at least 304 units, or max_gather_pages_per_unit <= 256): every unit gets S
- *     splits, S the largest power of two <= 16 with units * S <= two CTAs per SM; the
- *     S CTAs of a unit form one thread-block cluster and merge through distributed
+ * Split-KV: a unit's gathered pages are cut into contiguous pieces; each piece keeps an
+ * fp32 online softmax and the partials are merged by log-sum-exp in a fixed order, so
+ * the result does not depend on timing. Three plans, chosen from the dims:
+ *   - cluster mode (at most 19 units with max_gather_pages_per_unit <= 1024; for fp32
+ *     caches also at least 304 units, or max_gather_pages_per_unit <= 256): every unit
+ *     gets S splits, S the largest power of two <= 16 with units * S <= two CTAs per SM;
+ *     the S CTAs of a unit form one thread-block cluster and merge through distributed
  *     shared memory; split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
- *   - workspace mode (otherwise): each unit's splits are sized by its own page count,
+ *   - balanced mode (bf16 caches otherwise, up to 1024 units): the selected pages of
+ *     all units, in unit order, form one stream of W pages, cut into P' = min(P, W)
+ *     equal contiguous shares, one per CTA of a persistent grid of P CTAs (as many as
+ *     fit on the GPU at once, at most 512); the pieces of a unit merge through split
+ *     records in the workspace, the last piece to finish merging them in CTA order;
+ *   - workspace mode (the rest): each unit's splits are sized by its own page count,
  *     p = max(4 * ceil(pages / 128), m) pages per split (m = 32, or 4 when
  *     max_gather_pages_per_unit > 1024), so at most 32 splits; partials go through the
- *     workspace and the last split to finish merges them (an int32 arrival counter per
- *     unit).
- * A sub-batch launched with the same S (or in workspace mode) gives bitwise the same
- * per-unit results as the full batch.
+ *     workspace and the last split to finish merges them.
+ * In cluster and workspace mode a unit's plan depends on its own sizes only, so a
+ * sub-batch launched with the same S gives bitwise the same per-unit results as the full
+ * batch; in balanced mode the shares depend on every unit's page count, so a sub-batch
+ * can differ from the full batch in the last bits of the attention output (never in a
+ * selection), while repeated runs on the same inputs are bitwise equal.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
- * aligned. It starts with two int32 arrival counters per unit (padded to 16 bytes);
- * these must be zero before the first call: zero the workspace once after
- * allocating it. Every call that completes leaves them zero again; after a call
- * that reported BS_ERR_TIMEOUT, zero them again. The rest is overwritten per call.
+ * aligned. It starts with four int32 words per unit (padded to 16 bytes): the fused
+ * step's selection tickets, the attention's arrival tickets, the fused step's published
+ * selections and the epochs of the last ones taken. These must be zero before the first
+ * call: zero the workspace once after allocating it. Every call that completes leaves
+ * the tickets zero again; after a call that reported BS_ERR_TIMEOUT, zero the workspace
+ * again. Then, by mode: cluster mode the fused step's page lists (int32 [units]
+ * [max_gather_pages_per_unit]); balanced mode the page lists, then one split record of
+ * G * (head_dim + 4) floats per (unit + CTA) for units + 512 records; workspace mode 32
+ * split records per unit. The rest is overwritten per call.
  * Calls that share a workspace must not run concurrently. */
 bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
                                 const bs_head_cfg *cfg, const int32_t *sel_idx,
@@ -230,11 +240,9 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * inside this library's device memory, which every GPU that loads the library keeps
  * until the process exits.
  * Limit: bs_workspace_size(dims) must not exceed 8 MiB; larger dims return
- * BS_ERR_CAPACITY before anything is enqueued. Where the split partials go through the
- * workspace (selections above 1024 pages, or 20 to 303 units with selections above 256
- * pages) that is 67.6 KB per unit at head_dim 128 and G = 4: at most 124 units (62 at
- * G = 8). In cluster mode the counters and the fused step's page lists take
- * 8 + 4 * max_gather_pages_per_unit bytes per unit (2,044 units at 1024 pages).
+ * BS_ERR_CAPACITY before anything is enqueued. At head_dim 128 with bf16 caches in
+ * balanced mode that allows, with 1024 pages per unit, all 1,024 units of the plan at
+ * G = 4 (746 at G = 8); with 2048 pages per unit, 708 units at G = 4 (500 at G = 8).
  * The first call on each device looks up the array's device address with that device
  * current and caches it; make that first call before any stream capture. The cached
  * address belongs to the device's context at that time: after cudaDeviceReset (or
@@ -286,11 +294,13 @@ typedef struct {
  * Launch 1 scores every candidate tile (one or several 64-row tiles per CTA); the
  * unit's first CTA also updates a1 (that sub-block lies in the forced tail block,
  * which no score of this step reads); the unit's CTA that finishes last (an arrival
- * ticket) selects, publishes the selection (cur_cnt is set to -1 first and receives
- * the count with a release store once the row and the page list are written) and
- * writes the set-difference. Launch 2 is the attention, launched as a programmatic
- * dependent: streaming units' splits start before launch 1 ends; the others wait,
- * bounded, for their unit's published count.
+ * ticket) selects, publishes the selection (once the row and the page list are
+ * written, cur_cnt receives the count and the unit's published word in the workspace
+ * receives (epoch << 16) | count with a release store, the epoch one past the one the
+ * attention last took, so a count left from an earlier step can never be taken for
+ * this step's) and writes the set-difference. Launch 2 is the attention, launched as a
+ * programmatic dependent: streaming units' pages need no selection and are attended
+ * before launch 1 ends; the others wait, bounded, for their unit's published word.
  * Both launches may begin before the work ahead of them in `stream` has finished;
  * before waiting for it they read only the per-unit head configuration (cfg arrays),
  * so those must not be written by the kernel immediately before this call. Everything
@@ -394,6 +404,18 @@ bs_status bs_lse_merge(const bs_dims *dims, const float *out_a, const float *lse
 
 /* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
 size_t bs_workspace_size(const bs_dims *dims);
+
+/* Every wait inside a kernel (for a bulk copy to land, for the fused step's selection
+ * to be published) gives up after a wall-clock limit, reports BS_ERR_TIMEOUT in the
+ * status word and lets the kernel finish. This sets that limit, in nanoseconds, for the
+ * kernels launched from now on (those already captured in a CUDA graph keep the limit
+ * they were captured with); 1000 ns .. 60 s, default one second. Returns
+ * BS_ERR_INVALID_ARG (and keeps the old limit) outside that range. Process-wide; host
+ * only. */
+bs_status bs_set_wait_limit_ns(uint64_t limit_ns);
+
+/* The current limit of device-side waits, in nanoseconds. */
+uint64_t bs_wait_limit_ns(void);
 
 /* Static text for a status code. */
 const char *bs_status_string(bs_status status);

@@ -110,6 +110,8 @@ _SIGS = {
     "bs_lse_merge": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
+    "bs_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
+    "bs_wait_limit_ns": (ctypes.c_uint64, []),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -242,3 +244,12 @@ def lse_merge(dims, out_a, lse_a, out_b, lse_b, out, lse, stream=None):
 
 def workspace_size(dims) -> int:
     return int(lib().bs_workspace_size(ctypes.byref(dims)))
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """Limit of every device-side wait of the calls launched from now on (default 1 s)."""
+    _check("bs_set_wait_limit_ns", lib().bs_set_wait_limit_ns(int(limit_ns)))
+
+
+def wait_limit_ns() -> int:
+    return int(lib().bs_wait_limit_ns())

@@ -1,5 +1,6 @@
 // Host-side parts of the C ABI that launch nothing: status text, shape checks,
 // head-configuration checks and workspace sizing.
+#include <atomic>
 #include <climits>
 #include <cstdint>
 
@@ -7,6 +8,12 @@
 #include "bs_internal.cuh"
 
 namespace bsi {
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 bs_status check_dims(const bs_dims *d) {
   if (d == nullptr) return BS_ERR_INVALID_ARG;
@@ -71,6 +78,14 @@ bs_status make_kv_tensor_maps(const bs_dims &d, const bs_kv &kv, CUtensorMap *tk
 
 extern "C" {
 
+bs_status bs_set_wait_limit_ns(uint64_t limit_ns) {
+  if (limit_ns < 1000 || limit_ns > 60000000000ull) return BS_ERR_INVALID_ARG;
+  bsi::g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  return BS_OK;
+}
+
+uint64_t bs_wait_limit_ns(void) { return bsi::wait_limit_ns(); }
+
 const char *bs_status_string(bs_status s) {
   switch (s) {
     case BS_OK: return "ok";
@@ -89,12 +104,14 @@ size_t bs_workspace_size(const bs_dims *dims) {
   if (bsi::check_dims(dims) != BS_OK) return 0;
   const int G = dims->n_q_heads / dims->n_kv_heads;
   const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
+  const int mg = dims->max_gather_pages_per_unit;
   // Cluster mode keeps the split partials on chip: the counters and the fused step's
-  // page lists. Workspace mode: the counters and the split records.
-  const size_t tail = bsi::attn_cluster_mode(static_cast<int>(units), dims->max_gather_pages_per_unit)
-                          ? bsi::attn_plist_ints(units, dims->max_gather_pages_per_unit)
-                          : units * bsi::kAttnMaxSplits * G * bsi::attn_record_floats(dims->head_dim);
-  return (bsi::attn_counter_floats(units) + tail) * sizeof(float);
+  // page lists. Balanced mode: the counters, the page lists and one split record per
+  // (unit + CTA). Workspace mode: the counters and 32 split records per unit.
+  const int mode = bsi::attn_mode(static_cast<int>(units), mg, dims->kv_dtype);
+  const size_t head = mode == bsi::kModeCluster ? bsi::attn_counter_floats(units) + bsi::attn_plist_ints(units, mg)
+                                                : bsi::attn_records_offset(units, mg, mode);
+  return (head + bsi::attn_record_area_floats(units, G, dims->head_dim, mode)) * sizeof(float);
 }
 
 bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *c, const int32_t *seq_lens_host) {

@@ -19,10 +19,15 @@ bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv,
   a.sel_cnt = sel_cnt;
   a.out = out;
   a.lse = lse;
-  a.arrivals = reinterpret_cast<int32_t *>(ws) + units;  // second counter of each unit
-  a.records = ws + attn_counter_floats(units);
+  const StepWords w = step_words(ws, units);
+  a.arrivals = w.arrivals;
+  a.records = ws + attn_records_offset(units, dims->max_gather_pages_per_unit,
+                                       attn_mode(units, dims->max_gather_pages_per_unit, dims->kv_dtype));
   a.plist = nullptr;
+  a.pub = nullptr;
+  a.expect = nullptr;
   a.st = st;
+  a.wait_ns = wait_limit_ns();
   return dims->kv_dtype == BS_BF16 ? launch_attn_bf16(a, false, cs) : launch_attn_f32(a, false, cs);
 }
 

@@ -10,8 +10,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kFfmaThreads) attn_ffma_kernel(AttnArgs a, bool step, bool cluster) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (step) pdl_launch_dependents();
-  attn_split_ffma<D, G>(a.dims, a.q, a.kv, a.cfg, a.sel_idx, a.sel_cnt, a.plist, a.arrivals, a.records, a.out, a.lse, a.st,
-                        smem, step, cluster);
+  attn_split_ffma<D, G>(a, smem, step, cluster);
   if (step) pdl_wait();
 }
 
@@ -24,7 +23,7 @@ bs_status launch_modes(const AttnArgs &a, bool step, cudaStream_t cs) {
       cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (!attrs_ok) return BS_ERR_CUDA;
   const int units = a.dims.batch * a.dims.n_kv_heads;
-  const bool cluster = attn_cluster_mode(units, a.dims.max_gather_pages_per_unit);
+  const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit, BS_FP32) == kModeCluster;
   const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
   const dim3 grid(splits, units);
   const cudaError_t e =

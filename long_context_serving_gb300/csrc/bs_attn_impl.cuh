@@ -43,6 +43,7 @@
 #include <cuda.h>
 #include <math.h>
 
+#include "bs_attn_launch.cuh"
 #include "bs_attn_plan.cuh"
 #include "bs_internal.cuh"
 
@@ -92,6 +93,8 @@ struct UnitBlocks {
   const int32_t *sel;     // selection row (global), when not computed
   const int32_t *sel_sm;  // its first kSelPreload entries in shared memory
   const int32_t *plist;   // the unit's page list (fused step), or null
+  bool polled;            // the count came from the fused step's published word
+  int epoch;              // the epoch that word carried
   UnitPages pg;
 
   __device__ __forceinline__ int block(int i) const {
@@ -102,10 +105,38 @@ struct UnitBlocks {
 
 // Reads a unit's block list (waiting for the selection kernel in step mode unless
 // the unit is streaming) and its split plan. All NT threads call it.
+// Waits (bounded by wait_ns) until the fused step's front kernel has published unit
+// u's selection for this step: the published word carries the epoch after the one in
+// expect[u] (which the attention advances once every reader of the unit is done).
+// Returns the count, or 0 after reporting BS_ERR_TIMEOUT; *epoch gets the epoch.
+// Relaxed polls with a short sleep, then one acquire fence, so the row and the page
+// list written before the release store are visible.
+__device__ __forceinline__ int wait_published(const int32_t *pub, const int32_t *expect, int u, uint64_t wait_ns,
+                                              int32_t *st, int *epoch) {
+  const int e = (__ldcg(expect + u) + 1) & kEpochMask;
+  *epoch = e;
+  int w = load_relaxed_gpu(pub + u);
+  if ((w >> 16) != e) {
+    const uint64_t t0 = global_ns();
+    while (((w = load_relaxed_gpu(pub + u)) >> 16) != e) {
+      __nanosleep(64);
+      if (global_ns() - t0 > wait_ns) {
+        report(st, BS_ERR_TIMEOUT);
+        return 0;
+      }
+    }
+  }
+  fence_acq_rel_gpu();
+  return w & 0xffff;
+}
+
 template <int NT>
-__device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
-                                       const int32_t *sel_idx, const int32_t *sel_cnt, const int32_t *plist, int u,
-                                       int32_t *sel_sm, int32_t *st, bool in_step, bool in_cluster) {
+__device__ UnitBlocks load_unit_blocks(const AttnArgs &a, int u, int32_t *sel_sm, bool in_step, bool in_cluster) {
+  const bs_dims &dims = a.dims;
+  const bs_kv &kv = a.kv;
+  const bs_head_cfg &cfg = a.cfg;
+  const int32_t *sel_idx = a.sel_idx, *sel_cnt = a.sel_cnt, *plist = a.plist;
+  int32_t *st = a.st;
   __shared__ int sh_cnt;
   const int tid = threadIdx.x, split = blockIdx.x;
   const int b = u / dims.n_kv_heads;
@@ -116,6 +147,8 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
   ub.sel = sel_idx + static_cast<size_t>(u) * dims.max_sel_per_unit;
   ub.sel_sm = sel_sm;
   ub.plist = nullptr;
+  ub.polled = false;
+  ub.epoch = 0;
   ub.n_sink = ub.lo2 = 0;
   ub.cnt = 0;
   const bool cfg_ok = ub.g > 0 && ub.g % kPage == 0 && ub.T >= 1;
@@ -135,27 +168,16 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
     __syncthreads();
     ub.cnt = sh_cnt;
   } else if (!ub.computed) {
+    __shared__ int sh_epoch;
     if (tid == 0) {
-      // The selection kernel publishes this unit's count with a release store once the
-      // row is written (-1 until then): poll with relaxed loads and a short sleep, then
-      // one acquire fence. Bounded wait: about one second.
-      int c = load_relaxed_gpu(sel_cnt + u);
-      if (c < 0) {
-        const uint64_t t0 = global_ns();
-        while ((c = load_relaxed_gpu(sel_cnt + u)) < 0) {
-          __nanosleep(64);
-          if (global_ns() - t0 > 1000000000ull) {
-            report(st, BS_ERR_TIMEOUT);
-            c = 0;
-            break;
-          }
-        }
-      }
-      fence_acq_rel_gpu();
-      sh_cnt = c;
+      int e = 0;
+      sh_cnt = wait_published(a.pub, a.expect, u, a.wait_ns, st, &e);
+      sh_epoch = e;
     }
     __syncthreads();
     ub.cnt = sh_cnt;
+    ub.polled = true;
+    ub.epoch = sh_epoch;
     if (plist != nullptr) {
       // The selection kernel also wrote the pages of the selected blocks; the last
       // selected block is the tail block, which is always forced.
@@ -183,17 +205,6 @@ __device__ UnitBlocks load_unit_blocks(const bs_dims &dims, const bs_kv &kv, con
     ub.pg.n_pages = 0;
   }
   return ub;
-}
-
-// Zero output and lse = -inf for a unit with nothing to attend (split 0 writes).
-template <int NT, int D, int G>
-__device__ void write_empty_output(float *out, float *lse, size_t orow0) {
-  constexpr int QD = D / 4;
-  if (blockIdx.x != 0) return;
-  for (int i = threadIdx.x; i < G * QD; i += NT) {
-    reinterpret_cast<float4 *>(out + (orow0 + i / QD) * D)[i % QD] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i % QD == 0) lse[orow0 + i / QD] = -INFINITY;
-  }
 }
 
 // Resolves page slot `lane` (< kStagePages) of a stage: returns the physical page and
@@ -230,28 +241,44 @@ __device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims 
   return min(kPage, ub.T - t0);
 }
 
-// Epilogue shared by both paths. `o_sm` holds this split's unnormalised output
-// [G][D] (fp32, shared), `m_sm`/`l_sm` its per-head max (log2 units) and sum. A
-// single split writes out/lse; otherwise the record is published, a ticket taken and
-// the last split merges all records in split order. `scratch` needs
-// 3 * kMaxG * kAttnMaxSplits floats of shared memory. All NT threads call it.
+// Output row of one head from an unnormalised state (o, m in log2 units, l): o / l and
+// lse = ln 2 (m + log2 l); a state with l = 0 (nothing attended) gives a zero row and
+// lse = -inf.
+__device__ __forceinline__ void write_normalised(float4 o, float m, float l, float *orow, float *lse_h, int dq) {
+  if (l > 0.0f) {
+    const float inv = 1.0f / l;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+  } else {
+    o = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  reinterpret_cast<float4 *>(orow)[dq] = o;
+  if (dq == 0) *lse_h = l > 0.0f ? (m + log2f(l)) * kLn2 : -INFINITY;
+}
+
+// Epilogue of the workspace mode, shared by both paths. `o_sm` holds this split's
+// unnormalised output [G][D] (fp32, shared), `m_sm`/`l_sm` its per-head max (log2
+// units) and sum. A launch with one split per unit writes out/lse; otherwise every
+// launched split (an idle one with an empty state) publishes its record and takes a
+// ticket, and the last of the gridDim.x splits merges all records in split order and,
+// in the fused step, advances the unit's epoch (every split has read it by then).
+// `scratch` needs 3 * kMaxG * kAttnMaxSplits floats of shared memory. All NT threads
+// call it.
 template <int NT, int D, int G>
 __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const float *o_sm, const float *m_sm,
-                             const float *l_sm, int32_t *arrivals, float *ws, float *out, float *lse, float *scratch) {
+                             const float *l_sm, int32_t *arrivals, float *ws, float *out, float *lse, float *scratch,
+                             int32_t *expect) {
   constexpr int QD = D / 4;
   constexpr int REC = attn_record_floats(D);
   __shared__ int is_last;
   __shared__ float ML[2][kMaxG];
   const int tid = threadIdx.x, split = blockIdx.x;
-  if (ub.pg.n_split == 1) {
+  if (gridDim.x == 1) {
     for (int i = tid; i < G * QD; i += NT) {
       const int h = i / QD, dq = i % QD;
-      float4 o = reinterpret_cast<const float4 *>(o_sm + h * D)[dq];
-      const float inv = 1.0f / l_sm[h];
-      o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-      reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
-      if (dq == 0) lse[orow0 + h] = (m_sm[h] + log2f(l_sm[h])) * kLn2;
+      write_normalised(reinterpret_cast<const float4 *>(o_sm + h * D)[dq], m_sm[h], l_sm[h], out + (orow0 + h) * D,
+                       lse + orow0 + h, dq);
     }
+    if (ub.polled && tid == 0) expect[u] = ub.epoch;
     return;
   }
   float *rec = ws + (static_cast<size_t>(u) * kAttnMaxSplits + split) * G * REC;
@@ -266,12 +293,12 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
   // Publish the record and take an arrival ticket: the CTA barrier orders every
   // thread's record writes before thread 0's release; the last split acquires.
   __syncthreads();
-  if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == ub.pg.n_split - 1);
+  const int ns = static_cast<int>(gridDim.x);
+  if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == ns - 1);
   __syncthreads();
   if (!is_last) return;
   // Merge: M = max m_i, L = sum l_i 2^(m_i - M), o = sum 2^(m_i - M) o_i / L,
   // lse = ln 2 (M + log2 L); splits are visited in index order.
-  const int ns = ub.pg.n_split;
   const float *base = ws + static_cast<size_t>(u) * kAttnMaxSplits * G * REC;
   float *m_all = scratch;                          // [G][32]
   float *l_all = m_all + kMaxG * kAttnMaxSplits;
@@ -317,12 +344,12 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
           o.w = fmaf(v[j].w, w, o.w);
         }
     }
-    const float inv = 1.0f / ML[1][h];
-    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
-    if (dq == 0) lse[orow0 + h] = (ML[0][h] + log2f(ML[1][h])) * kLn2;
+    write_normalised(o, ML[0][h], ML[1][h], out + (orow0 + h) * D, lse + orow0 + h, dq);
   }
-  if (tid == 0) arrivals[u] = 0;  // ready for the next call
+  if (tid == 0) {
+    arrivals[u] = 0;  // ready for the next call
+    if (ub.polled) expect[u] = ub.epoch;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -391,10 +418,7 @@ __device__ void cluster_merge_c(size_t orow0, const float *o_sm, const float *m_
       o.z = fmaf(v[p].z, w, o.z);
       o.w = fmaf(v[p].w, w, o.w);
     }
-    const float inv = 1.0f / Lsum;
-    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
-    if (dq == 0) lse[orow0 + h] = (M + log2f(Lsum)) * kLn2;
+    write_normalised(o, M, Lsum, out + (orow0 + h) * D, lse + orow0 + h, dq);
   }
   cluster_sync_all();
 }
@@ -414,12 +438,8 @@ __device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm
   }
   for (int i = threadIdx.x; i < NF4; i += NT) {
     const int h = i / QD, dq = i % QD;
-    const float L = l_sm[h];
-    const float inv = 1.0f / L;
-    float4 o = reinterpret_cast<const float4 *>(o_sm + h * D)[dq];
-    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-    reinterpret_cast<float4 *>(out + (orow0 + h) * D)[dq] = o;
-    if (dq == 0) lse[orow0 + h] = (m_sm[h] + log2f(L)) * kLn2;
+    write_normalised(reinterpret_cast<const float4 *>(o_sm + h * D)[dq], m_sm[h], l_sm[h], out + (orow0 + h) * D,
+                     lse + orow0 + h, dq);
   }
 }
 
@@ -461,19 +481,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// D = A B + C for m16n8k16, bf16 inputs, fp32 accumulators, keeping only rows 0..7.
-// Rows 8..15 of A are padding heads: their A registers are 0, their C inputs are 0 and
-// their D outputs go to dead temporaries, so they cost no live registers.
-#pragma nv_diag_suppress 550  // t2, t3 below are written by the MMA and deliberately unused
-__device__ __forceinline__ void mma_bf16(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  float t2, t3;
+// D = A B + D for m16n8k16, bf16 inputs, fp32 accumulators (row-major A, column-major B).
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %10, %10};"
-      : "+f"(d[0]), "+f"(d[1]), "=f"(t2), "=f"(t3)
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f));
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-#pragma nv_diag_default 550
+// Transpose of an 8x8 matrix of 16-bit values held one register per thread in the MMA
+// fragment layout (row lane/4, columns 2(lane%4), 2(lane%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -488,21 +511,179 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return static_cast<uint32_t>((c >> 3) * (kPage * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// The G query rows of a unit (starting at row orow0 of q) as MMA A fragments of one
+// warp: rows = heads, rows >= G are zero. For an fp32 query, `lo` carries the remainder
+// q - bf16(q) as a second set of bf16 fragments (zero for a bf16 query).
 template <int D, int G>
-__device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
-                               const bs_head_cfg &cfg, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                               const int32_t *__restrict__ sel_idx, const int32_t *__restrict__ sel_cnt,
-                               const int32_t *plist, int32_t *__restrict__ arrivals, float *__restrict__ ws,
-                               float *__restrict__ out,
-                               float *__restrict__ lse, int32_t *st, unsigned char *smem, bool in_step,
-                               bool in_cluster) {
+__device__ __forceinline__ void load_q_frags(const void *q, size_t orow0, bool q32, uint32_t (&hi)[D / 16][2],
+                                             uint32_t (&lo)[D / 16][2]) {
+  const int lane = threadIdx.x & 31;
+  const int hrow = lane >> 2, qcol = 2 * (lane & 3);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      hi[kk][j] = 0u;
+      lo[kk][j] = 0u;
+      if (hrow < G) {
+        const size_t idx = (orow0 + hrow) * D + kk * 16 + j * 8 + qcol;
+        if (!q32) {
+          hi[kk][j] = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(q) + idx);
+        } else {
+          const float2 qf = *reinterpret_cast<const float2 *>(static_cast<const float *>(q) + idx);
+          hi[kk][j] = pack_bf16(qf.x, qf.y);
+          lo[kk][j] = pack_bf16(qf.x - bf16_lo_f(hi[kk][j]), qf.y - bf16_hi_f(hi[kk][j]));
+        }
+      }
+    }
+}
+
+// One 16-token page of K and V (swizzled tiles in shared memory, kpg and vpg) into a
+// warp's online softmax state, with the tokens as the MMA rows and the heads as its
+// columns (m16n8k16, bf16 inputs, fp32 accumulation; up to 8 heads):
+//   S^T = K q^T      A = the page's K tile (16 tokens x 16 dims per k-step, ldmatrix),
+//                    B = q^T (qa_hi / qa_lo: the query fragments of load_q_frags);
+//   O^T += V^T P^T   A = V^T (16 dims x 16 tokens, transposed ldmatrix),
+//                    B = P^T (the probabilities transposed in registers with movmatrix).
+// P enters as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)), which keeps it to
+// about 2^-16 relative. Each thread holds the state of heads h = 2(lane%4) + {0, 1}:
+// m_run[], l_run[] (log2 units; replicated over the 8 lanes with equal lane%4) and
+// o[m][j] = O[head h(j)][dim 16m + lane/4 + 8 (j >> 1)], j = (j & 1) picking the head.
+// `valid` tokens (1..16) hold data: rows past it are zeroed in V and masked out of S.
+// Scores in log2 units (qk_scale = log2(e) / sqrt(d)). Called by all 32 lanes.
+template <int D>
+__device__ __forceinline__ void mma_page(unsigned char *kpg, unsigned char *vpg, int valid,
+                                         const uint32_t (&qa_hi)[D / 16][2], const uint32_t (&qa_lo)[D / 16][2],
+                                         bool q32, float qk_scale, float (&m_run)[2], float (&l_run)[2],
+                                         float (&o)[D / 16][4]) {
+  constexpr int KSTEPS = D / 16;
+  const int lane = threadIdx.x & 31;
+  if (valid < kPage) {
+    // Rows past T may hold anything (even NaN): zero them in V; their scores are
+    // masked below.
+    for (int i = lane; i < (kPage - valid) * (D / 8); i += 32) {
+      const int r = valid + i / (D / 8), c = i % (D / 8);
+      *reinterpret_cast<uint4 *>(vpg + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+  }
+  // ---- S^T = K q^T: two accumulators (even and odd k-steps) halve the MMA chain ---------
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t kbase = smem_u32(kpg);
+  const int lrow = ((lane >> 4) << 3) + (lane & 7);   // token row this lane addresses
+  const int lsub = (lane >> 3) & 1;                  // low / high 8 columns of the k-step
+#pragma unroll
+  for (int kk = 0; kk < KSTEPS; ++kk) {
+    uint32_t b0, b1, b2, b3;   // (tokens 0-7, cols 0-7), (0-7, 8-15), (8-15, 0-7), (8-15, 8-15)
+    ldsm_x4(kbase + swz(lrow, 2 * kk + lsub), b0, b1, b2, b3);
+    float (&acc)[4] = (kk & 1) ? s1 : s0;
+    mma_bf16(acc, b0, b2, b1, b3, qa_hi[kk][0], qa_hi[kk][1]);
+    if (q32) mma_bf16(acc, b0, b2, b1, b3, qa_lo[kk][0], qa_lo[kk][1]);
+  }
+  // ---- online softmax per head over the 16 tokens -----------------------------------
+  // x[j]: token lane/4 + 8 (j >> 1), head 2(lane%4) + (j & 1).
+  const int t0 = lane >> 2;
+  float x[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + 8 * (j >> 1);
+    x[j] = t < valid ? (s0[j] + s1[j]) * qk_scale : -INFINITY;
+  }
+  float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int o2 = 4; o2 < 32; o2 <<= 1) {
+    mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], o2));
+    mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], o2));
+  }
+  float alpha[2], p[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float m_new = fmaxf(m_run[h], mx[h]);
+    alpha[h] = m_new == -INFINITY ? 1.0f : exp2f(m_run[h] - m_new);
+    p[h] = m_new == -INFINITY ? 0.0f : exp2f(x[h] - m_new);
+    p[h + 2] = m_new == -INFINITY ? 0.0f : exp2f(x[h + 2] - m_new);
+    m_run[h] = m_new;
+  }
+  float ps[2] = {p[0] + p[2], p[1] + p[3]};
+#pragma unroll
+  for (int o2 = 4; o2 < 32; o2 <<= 1) {
+    ps[0] += __shfl_xor_sync(0xffffffffu, ps[0], o2);
+    ps[1] += __shfl_xor_sync(0xffffffffu, ps[1], o2);
+  }
+  l_run[0] = l_run[0] * alpha[0] + ps[0];
+  l_run[1] = l_run[1] * alpha[1] + ps[1];
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) {
+    o[m][0] *= alpha[0];
+    o[m][1] *= alpha[1];
+    o[m][2] *= alpha[0];
+    o[m][3] *= alpha[1];
+  }
+  // P^T as bf16 hi + lo B fragments: pack (token, head pair) rows, transpose the two 8x8
+  // blocks (tokens 0-7 and 8-15).
+  const uint32_t ph0 = pack_bf16(p[0], p[1]), ph1 = pack_bf16(p[2], p[3]);
+  const uint32_t pl0 = pack_bf16(p[0] - bf16_lo_f(ph0), p[1] - bf16_hi_f(ph0));
+  const uint32_t pl1 = pack_bf16(p[2] - bf16_lo_f(ph1), p[3] - bf16_hi_f(ph1));
+  const uint32_t bh0 = movmatrix_t(ph0), bh1 = movmatrix_t(ph1);
+  const uint32_t bl0 = movmatrix_t(pl0), bl1 = movmatrix_t(pl1);
+  // ---- O^T += V^T P^T: V^T fragments by transposed ldmatrix ------------------------------
+  const uint32_t vbase = smem_u32(vpg);
+  const int vrow = (lane & 7) + ((lane >> 4) << 3);  // token row this lane addresses
+  const int vsub = (lane >> 3) & 1;                  // which 8-dim half of the m-tile
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m) {
+    uint32_t a0, a1, a2, a3;   // V^T (dims 0-7, tokens 0-7), (8-15, 0-7), (0-7, 8-15), (8-15, 8-15)
+    ldsm_x4_t(vbase + swz(vrow, 2 * m + vsub), a0, a1, a2, a3);
+    mma_bf16(o[m], a0, a1, a2, a3, bh0, bh1);
+    mma_bf16(o[m], a0, a1, a2, a3, bl0, bl1);
+  }
+}
+
+// A warp's softmax state (after mma_page) into shared memory: m and l of heads < G at
+// mw[h], lw[h] (lanes 0-3 write).
+template <int G>
+__device__ __forceinline__ void store_warp_ml(const float (&m_run)[2], const float (&l_run)[2], float *mw, float *lw) {
+  const int lane = threadIdx.x & 31;
+  if (lane < 4) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int h = 2 * lane + j;
+      if (h < G) {
+        mw[h] = m_run[j];
+        lw[h] = l_run[j];
+      }
+    }
+  }
+}
+// A warp's O of heads < G into ow[h * D + d]: o * wt[h], added (fmaf) to what is there
+// when `accumulate`; wt = null stores o as it is.
+template <int D, int G>
+__device__ __forceinline__ void add_warp_o(const float (&o)[D / 16][4], const float *wt, float *ow, bool accumulate) {
+  const int lane = threadIdx.x & 31;
+  const int h0 = 2 * (lane & 3), d0 = lane >> 2;
+#pragma unroll
+  for (int m = 0; m < D / 16; ++m)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int h = h0 + (j & 1), d = 16 * m + d0 + 8 * (j >> 1);
+      if (h < G) {
+        float *dst = ow + h * D + d;
+        *dst = wt == nullptr ? o[m][j] : fmaf(o[m][j], wt[h], accumulate ? *dst : 0.0f);
+      }
+    }
+}
+
+template <int D, int G>
+__device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv, unsigned char *smem,
+                               bool in_step, bool in_cluster) {
   using L = MmaLayout<D>;
   constexpr int NT = kMmaThreads;
   constexpr int KSTEPS = D / 16;
-  constexpr int NTILES = D / 8;
   constexpr int R = L::kRing;
   __shared__ uint64_t bars[R];
   __shared__ int slot_valid[R][kStagePages];
+  const bs_dims &dims = a.dims;
+  int32_t *st = a.st;
 
   const int u = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -510,18 +691,16 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  prefetch_page_row<NT>(dims, kv, cfg, plist, u, in_step);
-  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
-  if (!ub.ok || ub.pg.n_pages == 0) {
-    write_empty_output<NT, D, G>(out, lse, orow0);
-    return;
-  }
-  // In cluster mode a split without pages stays to take part in the merge.
-  if (!in_cluster && split >= ub.pg.n_split) return;
-  const int gp0 = min(split * ub.pg.pps, ub.pg.n_pages);
-  const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
+  prefetch_page_row<NT>(dims, a.kv, a.cfg, a.plist, u, in_step);
+  const UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
+  // Every launched split of the unit takes part to the end (an idle one with an empty
+  // state): the merge needs all CTAs of a cluster, and in workspace mode the last split
+  // to arrive merges, after every split of the unit has read the unit's words.
+  const int n_pages = ub.ok ? ub.pg.n_pages : 0;
+  const int gp0 = min(split * ub.pg.pps, n_pages);
+  const int gp1 = min(gp0 + ub.pg.pps, n_pages);
   const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
-  const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
+  const int32_t *pt = a.kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
 
   if (tid == 0) {
 #pragma unroll
@@ -566,148 +745,48 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
   // Query rows as MMA A fragments (rows = heads; rows >= G are zero). For an fp32
   // query a second bf16 fragment carries the remainder q - bf16(q).
   const bool q32 = dims.q_dtype == BS_FP32;
-  const int hrow = lane >> 2, qcol = 2 * (lane & 3);
-  uint32_t *qlo_sm = reinterpret_cast<uint32_t *>(smem + L::kOffQlo);
-  uint32_t qa_hi[KSTEPS][2];
-#pragma unroll
-  for (int kk = 0; kk < KSTEPS; ++kk)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      qa_hi[kk][j] = 0u;
-      uint32_t lo = 0u;
-      if (hrow < G) {
-        const size_t idx = (orow0 + hrow) * D + kk * 16 + j * 8 + qcol;
-        if (!q32) {
-          qa_hi[kk][j] = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(q) + idx);
-        } else {
-          const float2 qf = *reinterpret_cast<const float2 *>(static_cast<const float *>(q) + idx);
-          qa_hi[kk][j] = pack_bf16(qf.x, qf.y);
-          lo = pack_bf16(qf.x - bf16_lo_f(qa_hi[kk][j]), qf.y - bf16_hi_f(qa_hi[kk][j]));
-        }
-      }
-      if (q32 && warp == 0) qlo_sm[(kk * 2 + j) * 32 + lane] = lo;
-    }
-  if (q32) __syncthreads();
+  uint32_t qa_hi[KSTEPS][2], qa_lo[KSTEPS][2];
+  load_q_frags<D, G>(a.q, orow0, q32, qa_hi, qa_lo);
   const float qk_scale = rsqrtf(static_cast<float>(D)) * kLog2e;
 
-  float m_run = -INFINITY, l_run = 0.0f;   // head hrow (replicated over the lane quad)
-  float o[NTILES][2];   // O[head hrow][nd*8 + qcol + {0,1}]
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};   // heads 2(lane%4) + {0, 1}
+  float o[D / 16][4];
 #pragma unroll
-  for (int nd = 0; nd < NTILES; ++nd) o[nd][0] = o[nd][1] = 0.0f;
+  for (int m = 0; m < D / 16; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.0f;
 
+  int failed_at = -1;
   for (int it = 0; it < n_stages; ++it) {
     const int buf = it % R;
-    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it / R) & 1), st);
+    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it / R) & 1), st, a.wait_ns);
     // A copy that never lands: stop computing but still reach the merge (the status
     // word holds BS_ERR_TIMEOUT and the output is not meaningful).
-    if (__syncthreads_or(!ok)) break;
+    if (__syncthreads_or(!ok)) {
+      failed_at = it;
+      break;
+    }
     const int valid = slot_valid[buf][warp];
     if (valid > 0) {
       unsigned char *kpg = smem + buf * L::kBufBytes + warp * L::kPageBytes;
-      unsigned char *vpg = kpg + L::kStageKV;
-      if (valid < kPage) {
-        // Rows past T may hold anything (even NaN): zero them in V; their scores are
-        // masked below.
-        for (int i = lane; i < (kPage - valid) * (D / 8); i += 32) {
-          const int r = valid + i / (D / 8), c = i % (D / 8);
-          *reinterpret_cast<uint4 *>(vpg + swz(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        __syncwarp();
-      }
-      // ---- S = q K^T for the 16 tokens (two n-tiles of 8) ----------------------
-      float s[2][2];   // S[head hrow][nt*8 + qcol + {0,1}]
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = 0.0f;
-      const uint32_t kbase = smem_u32(kpg);
-      const int lrow = ((lane >> 4) << 3) + (lane & 7);   // token row this lane addresses
-      const int lsub = (lane >> 3) & 1;                  // low / high 8 columns of the k-step
-#pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz(lrow, 2 * kk + lsub), b0, b1, b2, b3);
-        mma_bf16(s[0], qa_hi[kk][0], qa_hi[kk][1], b0, b1);
-        mma_bf16(s[1], qa_hi[kk][0], qa_hi[kk][1], b2, b3);
-        if (q32) {
-          const uint32_t l0 = qlo_sm[(kk * 2) * 32 + lane], l1 = qlo_sm[(kk * 2 + 1) * 32 + lane];
-          mma_bf16(s[0], l0, l1, b0, b1);
-          mma_bf16(s[1], l0, l1, b2, b3);
-        }
-      }
-      // ---- online softmax over this page (rows = heads, quad = 16 tokens) -------
-      float x[2][2];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const int t = nt * 8 + qcol + j;
-          x[nt][j] = t < valid ? s[nt][j] * qk_scale : -INFINITY;
-          mx = fmaxf(mx, x[nt][j]);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run, mx);
-      float alpha = 1.0f, psum = 0.0f;
-      float p[2][2];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int j = 0; j < 2; ++j) p[nt][j] = 0.0f;
-      if (m_new != -INFINITY) {
-        alpha = exp2f(m_run - m_new);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            p[nt][j] = exp2f(x[nt][j] - m_new);
-            psum += p[nt][j];
-          }
-      }
-      psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-      psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-#pragma unroll
-      for (int nd = 0; nd < NTILES; ++nd) {
-        o[nd][0] *= alpha;
-        o[nd][1] *= alpha;
-      }
-      // P as bf16 hi + lo A fragments (k = the 16 tokens).
-      const uint32_t ph0 = pack_bf16(p[0][0], p[0][1]);
-      const uint32_t ph1 = pack_bf16(p[1][0], p[1][1]);
-      const uint32_t pl0 = pack_bf16(p[0][0] - bf16_lo_f(ph0), p[0][1] - bf16_hi_f(ph0));
-      const uint32_t pl1 = pack_bf16(p[1][0] - bf16_lo_f(ph1), p[1][1] - bf16_hi_f(ph1));
-      // ---- O += P V: V^T fragments by transposed ldmatrix -----------------------
-      const uint32_t vbase = smem_u32(vpg);
-      const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);   // token row this lane addresses
-      const int vsub = lane >> 4;                            // which of two 8-column chunks
-#pragma unroll
-      for (int nd2 = 0; nd2 < NTILES / 2; ++nd2) {
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vbase + swz(vrow, 2 * nd2 + vsub), v0, v1, v2, v3);
-        mma_bf16(o[2 * nd2], ph0, ph1, v0, v1);
-        mma_bf16(o[2 * nd2], pl0, pl1, v0, v1);
-        mma_bf16(o[2 * nd2 + 1], ph0, ph1, v2, v3);
-        mma_bf16(o[2 * nd2 + 1], pl0, pl1, v2, v3);
-      }
+      mma_page<D>(kpg, kpg + L::kStageKV, valid, qa_hi, qa_lo, q32, qk_scale, m_run, l_run, o);
     }
     __syncthreads();
     if (warp == 0 && it + R < n_stages) issue(it + R, buf);
+  }
+  if (failed_at >= 0) {
+    // Stages failed_at .. failed_at + R - 1 were issued and not consumed: wait (bounded)
+    // for their copies before the buffers are reused below or the CTA exits.
+    if (tid == 0)
+      for (int s2 = failed_at; s2 < min(n_stages, failed_at + R); ++s2)
+        mbar_wait_bounded(&bars[s2 % R], static_cast<uint32_t>((s2 / R) & 1), st, a.wait_ns);
+    __syncthreads();
   }
 
   // ---- combine the four warps' states ---------------------------------------------
   float *ow = reinterpret_cast<float *>(smem);               // [4][8][D] in buffer 0
   float *mw = ow + 4 * kMaxG * D;                            // [4][8]
   float *lw = mw + 4 * kMaxG;                                // [4][8]
-  if (hrow < G) {
-#pragma unroll
-    for (int nd = 0; nd < NTILES; ++nd)
-      *reinterpret_cast<float2 *>(ow + (warp * kMaxG + hrow) * D + nd * 8 + qcol) = make_float2(o[nd][0], o[nd][1]);
-    if ((lane & 3) == 0) {
-      mw[warp * kMaxG + hrow] = m_run;
-      lw[warp * kMaxG + hrow] = l_run;
-    }
-  }
+  add_warp_o<D, G>(o, nullptr, ow + warp * kMaxG * D, false);
+  store_warp_ml<G>(m_run, l_run, mw + warp * kMaxG, lw + warp * kMaxG);
   __syncthreads();
   __shared__ float mfin[kMaxG], lfin[kMaxG], wfin[4][kMaxG];
   if (tid < G) {
@@ -742,11 +821,14 @@ __device__ void attn_split_mma(const bs_dims &dims, const void *__restrict__ q, 
     reinterpret_cast<float4 *>(osum + h * D)[dq] = acc;
   }
   __syncthreads();
-  if (in_cluster)
-    cluster_merge<NT, D, G>(orow0, osum, mfin, lfin, out, lse);
-  else
-    finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, arrivals, ws, out, lse,
-                           reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4));
+  if (in_cluster) {
+    cluster_merge<NT, D, G>(orow0, osum, mfin, lfin, a.out, a.lse);
+    // Every CTA of the cluster has read the unit's words: advance its epoch.
+    if (ub.polled && split == 0 && tid == 0) a.expect[u] = ub.epoch;
+  } else {
+    finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, a.arrivals, a.records, a.out, a.lse,
+                           reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4), a.expect);
+  }
 }
 
 // ===========================================================================
@@ -770,13 +852,12 @@ struct FfmaLayout {
 };
 
 template <int D, int G>
-__device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q, const bs_kv &kv,
-                                const bs_head_cfg &cfg, const int32_t *__restrict__ sel_idx,
-                                const int32_t *__restrict__ sel_cnt, const int32_t *plist,
-                                int32_t *__restrict__ arrivals,
-                                float *__restrict__ ws, float *__restrict__ out, float *__restrict__ lse,
-                                int32_t *st, unsigned char *smem, bool in_step, bool in_cluster) {
+__device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_step, bool in_cluster) {
   using L = FfmaLayout<D, G>;
+  const bs_dims &dims = a.dims;
+  const bs_kv &kv = a.kv;
+  const void *q = a.q;
+  int32_t *st = a.st;
   constexpr int NT = kFfmaThreads;
   constexpr int DPL = D / 32;
   constexpr int kPer = D / 16;  // 16-byte chunks per quarter of a row (fp32: D/4 chunks per row)
@@ -790,15 +871,12 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
 
-  prefetch_page_row<NT>(dims, kv, cfg, plist, u, in_step);
-  const UnitBlocks ub = load_unit_blocks<NT>(dims, kv, cfg, sel_idx, sel_cnt, plist, u, sel_sm, st, in_step, in_cluster);
-  if (!ub.ok || ub.pg.n_pages == 0) {
-    write_empty_output<NT, D, G>(out, lse, orow0);
-    return;
-  }
-  if (!in_cluster && split >= ub.pg.n_split) return;
-  const int gp0 = min(split * ub.pg.pps, ub.pg.n_pages);
-  const int gp1 = min(gp0 + ub.pg.pps, ub.pg.n_pages);
+  prefetch_page_row<NT>(dims, kv, a.cfg, a.plist, u, in_step);
+  const UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
+  // Every launched split takes part to the end (see attn_split_mma).
+  const int n_pages = ub.ok ? ub.pg.n_pages : 0;
+  const int gp0 = min(split * ub.pg.pps, n_pages);
+  const int gp1 = min(gp0 + ub.pg.pps, n_pages);
   const int n_stages = (gp1 - gp0 + kStagePages - 1) / kStagePages;
   const int32_t *pt = kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
   const unsigned char *kpool = static_cast<const unsigned char *>(kv.k_pool);
@@ -849,10 +927,14 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
     for (int j = 0; j < DPL; ++j) acc[h][j] = 0.0f;
 
   const int tok = tid >> 2, qq = tid & 3;
+  int failed_at = -1;
   for (int it = 0; it < n_stages; ++it) {
     const int buf = it & 1;
-    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st);
-    if (__syncthreads_or(!ok)) break;
+    const bool ok = mbar_wait_bounded(&bars[buf], static_cast<uint32_t>((it >> 1) & 1), st, a.wait_ns);
+    if (__syncthreads_or(!ok)) {
+      failed_at = it;
+      break;
+    }
 
     const unsigned char *Kb = smem + buf * L::kStageBytes;
     const bool tvalid = (tok & (kPage - 1)) < slot_valid[buf][tok >> 4];
@@ -940,6 +1022,13 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
     __syncthreads();
     if (warp == 0 && it + 2 < n_stages) issue(it + 2, buf);
   }
+  if (failed_at >= 0) {
+    // Wait (bounded) for the copies still in flight before the buffers are reused.
+    if (tid == 0)
+      for (int s2 = failed_at; s2 < min(n_stages, failed_at + 2); ++s2)
+        mbar_wait_bounded(&bars[s2 & 1], static_cast<uint32_t>((s2 >> 1) & 1), st, a.wait_ns);
+    __syncthreads();
+  }
 
   // ---- sum the 8 warps' accumulators --------------------------------------------
   float *red = reinterpret_cast<float *>(smem);        // [8][G][D] over the K stages
@@ -961,11 +1050,13 @@ __device__ void attn_split_ffma(const bs_dims &dims, const void *__restrict__ q,
     osum[h * D + dd] = sum;
   }
   __syncthreads();
-  if (in_cluster)
-    cluster_merge<NT, D, G>(orow0, osum, ml_sm[0], ml_sm[1], out, lse);
-  else
-    finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], arrivals, ws, out, lse,
-                           reinterpret_cast<float *>(smem + 2 * L::kStageBytes));
+  if (in_cluster) {
+    cluster_merge<NT, D, G>(orow0, osum, ml_sm[0], ml_sm[1], a.out, a.lse);
+    if (ub.polled && split == 0 && tid == 0) a.expect[u] = ub.epoch;
+  } else {
+    finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], a.arrivals, a.records, a.out, a.lse,
+                           reinterpret_cast<float *>(smem + 2 * L::kStageBytes), a.expect);
+  }
 }
 
 }  // namespace bsi

@@ -15,10 +15,13 @@ struct AttnArgs {
   const int32_t *sel_cnt;
   float *out;
   float *lse;
-  int32_t *arrivals;  // per-unit counters (workspace mode)
-  float *records;     // split records (workspace mode)
-  const int32_t *plist;  // fused step, cluster mode: page lists of non-streaming units, else null
+  int32_t *arrivals;  // per-unit arrival tickets of the splits (workspace and balanced modes)
+  float *records;     // split records (workspace and balanced modes)
+  const int32_t *plist;  // fused step: page lists of non-streaming units, else null
+  const int32_t *pub;    // fused step: published selections, (epoch << 16) | count, per unit
+  int32_t *expect;       // fused step: epoch of the last selection the attention took, per unit
   int32_t *st;
+  uint64_t wait_ns;      // limit of every device-side wait
 };
 
 // step = true: launched as a programmatic dependent of the fused step's selection

@@ -15,19 +15,46 @@ constexpr int kAttnMaxSplits = 32;                 // splits of a unit in the wo
 // (unnormalised), m (log2 units), l, 2 pad.
 __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 
-// The workspace starts with two int32 arrival counters per unit (the selection phase
-// of the fused decode step, then the attention in workspace mode), padded to 16 bytes.
+// The workspace starts with four int32 words per unit, padded to 16 bytes:
+//   [0, U)    selection tickets of the fused step's front kernel;
+//   [U, 2U)   arrival tickets of the attention's splits;
+//   [2U, 3U)  the fused step's published selections: (epoch << 16) | count;
+//   [3U, 4U)  the epoch the next published selection carries, minus one (kept by the
+//             attention of the fused step).
 // After them: in cluster mode the fused step's page lists (int32 [units][max gather
-// pages]: the physical pages of each unit's selected blocks in attention order), in
-// workspace mode the split records.
-__host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (2 * units + 3) / 4 * 4; }
+// pages]: the physical pages of each unit's selected blocks in attention order); in
+// balanced mode the page lists, then the split records; in workspace mode the split
+// records.
+__host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (4 * units + 3) / 4 * 4; }
 __host__ __device__ constexpr size_t attn_plist_ints(size_t units, int max_gather) {
   return (units * static_cast<size_t>(max_gather) + 3) / 4 * 4;
+}
+constexpr int kEpochMask = 0x7fff;  // epochs of published selections wrap at 2^15
+
+// Counter words of unit u inside the workspace's first block.
+struct StepWords {
+  int32_t *tickets, *arrivals, *pub, *expect;
+};
+__host__ __device__ inline StepWords step_words(void *workspace, size_t units) {
+  int32_t *w = static_cast<int32_t *>(workspace);
+  return StepWords{w, w + units, w + 2 * units, w + 3 * units};
 }
 
 constexpr int kMidSplitPages = 32;   // workspace mode below 1024 pages: pages per split, at least
 constexpr int kClusterUnitsMax = 19; // cluster mode while units x 16 splits fit one wave of ~304 CTAs ...
 constexpr int kManyUnits = 304;      // ... or once the units alone fill it (then one split each)
+
+// Attention modes.
+//   cluster:   few units with small selections (bf16 and fp32 caches); a unit's S splits
+//              are one thread-block cluster and merge through distributed shared memory;
+//   balanced:  every other bf16 launch up to kWsMaxUnits units: the pages of all units
+//              form one stream cut into equal contiguous shares, one per CTA of a
+//              persistent grid; a unit's pieces merge through split records in the
+//              workspace (the last piece to finish merges);
+//   workspace: the rest (fp32 caches beyond cluster mode, bf16 beyond kWsMaxUnits).
+enum AttnMode { kModeCluster = 0, kModeBalanced = 1, kModeWorkspace = 2 };
+constexpr int kWsMaxUnits = 1024;  // units the balanced plan takes (page offsets in shared memory)
+constexpr int kWsMaxCtas = 512;    // CTAs of a balanced launch the record area is sized for
 
 // Cluster mode: a unit's splits are the CTAs of one cluster and merge through
 // distributed shared memory; every unit has the same number of splits. Workspace mode:
@@ -39,6 +66,26 @@ constexpr int kManyUnits = 304;      // ... or once the units alone fill it (the
 __host__ __device__ inline bool attn_cluster_mode(int units, int max_gather_pages) {
   if (max_gather_pages > kClusterMaxPages) return false;
   return units <= kClusterUnitsMax || units >= kManyUnits || max_gather_pages <= 8 * kMidSplitPages;
+}
+
+__host__ __device__ inline int attn_mode(int units, int max_gather_pages, int kv_dtype) {
+  if (kv_dtype == BS_BF16) {
+    if (units <= kClusterUnitsMax && max_gather_pages <= kClusterMaxPages) return kModeCluster;
+    if (units <= kWsMaxUnits) return kModeBalanced;
+  }
+  return attn_cluster_mode(units, max_gather_pages) ? kModeCluster : kModeWorkspace;
+}
+
+// Floats of the workspace before the split records (the counters, and the page lists
+// in balanced mode), and the floats of the records themselves.
+__host__ __device__ inline size_t attn_records_offset(size_t units, int max_gather_pages, int mode) {
+  return attn_counter_floats(units) + (mode == kModeBalanced ? attn_plist_ints(units, max_gather_pages) : 0);
+}
+__host__ __device__ inline size_t attn_record_area_floats(size_t units, int G, int D, int mode) {
+  const size_t rec = static_cast<size_t>(G) * (D + 4);
+  if (mode == kModeBalanced) return (units + kWsMaxCtas) * rec;   // index: unit + CTA
+  if (mode == kModeWorkspace) return units * 32 * rec;            // index: unit, split
+  return 0;
 }
 
 // Smallest split (pages) in workspace mode.

@@ -106,10 +106,13 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for a barrier phase with a wall-clock limit (about one second; the timer is
-// read every 64 tries only). Returns false and records BS_ERR_TIMEOUT if the phase
-// never completes.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *st) {
+// Default limit of every device-side wait (bs_set_wait_limit_ns changes it).
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // one second
+
+// Wait for a barrier phase with a wall-clock limit of limit_ns (the timer is read every
+// 64 tries only). Returns false and records BS_ERR_TIMEOUT if the phase never completes.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *st,
+                                                  uint64_t limit_ns = kDefaultWaitNs) {
   uint32_t n = 0;
   uint64_t t0 = 0;
   while (!mbar_try_wait(bar, parity)) {
@@ -117,13 +120,29 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
       const uint64_t t = global_ns();
       if (t0 == 0) {
         t0 = t;
-      } else if (t - t0 > 1000000000ull) {
+      } else if (t - t0 > limit_ns) {
         report(st, BS_ERR_TIMEOUT);
         return false;
       }
     }
   }
   return true;
+}
+
+// Plain arrival on a barrier (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id` (1..15;
+// 0 is the one __syncthreads uses).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Global -> shared bulk copy that signals `bar` with its byte count.
@@ -170,6 +189,9 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Shape checks common to every call. Returns BS_OK or the first problem.
 bs_status check_dims(const bs_dims *d);
+
+// The current limit of device-side waits in nanoseconds (bs_set_wait_limit_ns).
+uint64_t wait_limit_ns();
 
 // Tiled tensor maps over the bf16 K and V pools viewed as [n_pages * 16][head_dim]:
 // boxes of 16 rows x 64 columns (128 bytes) with 128-byte swizzle.

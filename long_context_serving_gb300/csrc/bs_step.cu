@@ -35,6 +35,15 @@ __device__ __forceinline__ void pdl_trigger_front() { asm volatile("griddepcontr
 __device__ __forceinline__ void store_release(int32_t *p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Publishes unit u's selection count for the attention: (epoch << 16) | count with a
+// release store, the epoch one past the one the attention last took (expect[u]; read
+// after the previous step's attention has finished, and written only by that attention
+// once every reader of the unit's word is done). A count that is not this step's cannot
+// match, whatever the timing.
+__device__ __forceinline__ void publish_selection(const StepWords &w, int u, int count) {
+  const int e = (__ldcg(w.expect + u) + 1) & kEpochMask;
+  store_release(w.pub + u, (e << 16) | count);
+}
 __device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
   int old;
   asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
@@ -60,7 +69,7 @@ __host__ __device__ inline size_t front_select_bytes(int max_blocks, int max_sel
 
 template <int D, int G>
 __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
-                                                                   bs_step_io io, int reduce, int32_t *arrivals,
+                                                                   bs_step_io io, int reduce, StepWords words,
                                                                    int32_t *plist, int pt_cache_ints, int tpc) {
   using L = ScoreLayout<D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -89,13 +98,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   // CTAs past every tile the unit can have leave before waiting.
   if (cj > 0 && (!scored || tile_row(t0) >= rows)) return;
   pdl_wait_front();  // q, lengths, KV pages, summaries and selection state are now final
-  // The attention reads a non-streaming unit's selection once its count is >= 0: mark
-  // it not ready before any attention CTA can start (the buffer's last readers, the
-  // previous step, have finished).
-  if (cj == 0 && tid == 0) {
-    io.cur_cnt[u] = -1;
-    __threadfence();
-  }
+  int32_t *arrivals = words.tickets;
   score_bars_init(bars, nbuf);
   __syncthreads();
   pdl_trigger_front();  // the attention may start launching
@@ -143,7 +146,8 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
         report(st, code);
         io.added_cnt[u] = 0;
         io.removed_cnt[u] = 0;
-        store_release(io.cur_cnt + u, 0);
+        io.cur_cnt[u] = 0;
+        publish_selection(words, u, 0);
       }
     }
     return;
@@ -264,7 +268,10 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   // Publish: the row and the page list are written; the count (release) tells the
   // attention they are ready.
   __syncthreads();
-  if (tid == 0) store_release(io.cur_cnt + u, total);
+  if (tid == 0) {
+    io.cur_cnt[u] = total;
+    publish_selection(words, u, total);
+  }
   cp_async_wait_all();
   __syncthreads();
   int np = np_sm;
@@ -291,8 +298,9 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
   if (!attr_ok) return BS_ERR_CUDA;
   const int units = dims.batch * dims.n_kv_heads;
-  const bool cluster = attn_cluster_mode(units, dims.max_gather_pages_per_unit);
-  int pt_cache = cluster && dims.max_pages_per_unit <= kPtCacheInts ? dims.max_pages_per_unit : 0;
+  const int mode = attn_mode(units, dims.max_gather_pages_per_unit, dims.kv_dtype);
+  const bool lists = mode != kModeWorkspace;   // the attention reads page lists
+  int pt_cache = lists && dims.max_pages_per_unit <= kPtCacheInts ? dims.max_pages_per_unit : 0;
   size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, pt_cache);
   if (front_smem > kFrontMaxSmem) {  // read the page table from global memory instead
     pt_cache = 0;
@@ -308,11 +316,11 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
   const int nbuf = tpc > 1 ? 2 : 1;
   if (front_smem < static_cast<size_t>(ScoreLayout<D, G>::bytes(nbuf))) front_smem = ScoreLayout<D, G>::bytes(nbuf);
   if (front_smem > kFrontMaxSmem) return BS_ERR_CAPACITY;
-  int32_t *counters = static_cast<int32_t *>(io.workspace);
-  int32_t *plist = cluster ? counters + attn_counter_floats(units) : nullptr;
+  const StepWords words = step_words(io.workspace, units);
+  int32_t *plist = lists ? words.tickets + attn_counter_floats(units) : nullptr;
   const dim3 front_grid(units, (max_tiles + tpc - 1) / tpc);
   if (launch_ex(step_front_kernel<D, G>, front_grid, kFrontThreads, front_smem, cs, 0, true, dims, kv, cfg, io,
-                reduce, counters, plist, pt_cache, tpc) != cudaSuccess)
+                reduce, words, plist, pt_cache, tpc) != cudaSuccess)
     return BS_ERR_CUDA;
   AttnArgs a;
   a.dims = dims;
@@ -323,10 +331,13 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
   a.sel_cnt = io.cur_cnt;
   a.out = io.out;
   a.lse = io.lse;
-  a.arrivals = counters + units;
-  a.records = static_cast<float *>(io.workspace) + attn_counter_floats(units);
+  a.arrivals = words.arrivals;
+  a.records = static_cast<float *>(io.workspace) + attn_records_offset(units, dims.max_gather_pages_per_unit, mode);
   a.plist = plist;
+  a.pub = words.pub;
+  a.expect = words.expect;
   a.st = io.dev_status;
+  a.wait_ns = wait_limit_ns();
   return dims.kv_dtype == BS_BF16 ? launch_attn_bf16(a, true, cs) : launch_attn_f32(a, true, cs);
 }
 

@@ -66,35 +66,45 @@ def test_pool_rows_stay_below_two_to_the_31():
         B.BS_ERR_CAPACITY
 
 
-def _ws(units, G, max_gather):
+def _ws(units, G, max_gather, kv=B.BS_BF16):
     return B.workspace_size(_dims(batch=1, n_kv_heads=units, n_q_heads=G * units,
-                                  max_gather_pages_per_unit=max_gather))
+                                  max_gather_pages_per_unit=max_gather, kv_dtype=kv))
 
 
 def test_workspace_size_modes():
-    """Two int32 counters per unit (padded to 16 bytes), then per unit either the fused
-    step's page list (cluster mode: 4 bytes per gathered page) or 32 split records of
-    G x (d + 4) floats (workspace mode), as the header states; and the 8 MiB limit of
-    the no-allocation call that follows from it."""
+    """Four int32 words per unit (padded to 16 bytes), then per mode as the header states:
+    cluster mode the fused step's page lists (4 bytes per gathered page); balanced mode
+    the page lists and one split record of G x (d + 4) floats per (unit + CTA), for up
+    to 512 CTAs; workspace mode 32 split records per unit. And the 8 MiB limit of the
+    no-allocation call that follows from it."""
     def counters(u):
-        return (2 * u + 3) // 4 * 4 * 4
-
-    def records(u, G):
-        return u * 32 * G * (128 + 4) * 4
+        return (4 * u + 3) // 4 * 4 * 4
 
     def plist(u, mg):
         return (u * mg + 3) // 4 * 4 * 4
 
-    assert _ws(8, 4, 1024) == counters(8) + plist(8, 1024)          # few units: cluster mode
-    assert _ws(8, 4, 2048) == counters(8) + records(8, 4)           # above 1024 pages
-    assert _ws(100, 4, 512) == counters(100) + records(100, 4)      # 20..303 units, > 256 pages
-    assert _ws(100, 4, 256) == counters(100) + plist(100, 256)
-    assert _ws(304, 4, 512) == counters(304) + plist(304, 512)      # many units: cluster mode again
+    def balanced(u, G, mg):
+        return counters(u) + plist(u, mg) + (u + 512) * G * (128 + 4) * 4
+
+    def workspace(u, G):
+        return counters(u) + u * 32 * G * (128 + 4) * 4
+
+    assert _ws(8, 4, 1024) == counters(8) + plist(8, 1024)          # few units, small selections: cluster
+    assert _ws(19, 4, 1024) == counters(19) + plist(19, 1024)
+    assert _ws(8, 4, 1025) == balanced(8, 4, 1025)                  # above 1024 pages
+    assert _ws(20, 4, 16) == balanced(20, 4, 16)                    # more than 19 units
+    assert _ws(1024, 7, 512) == balanced(1024, 7, 512)
+    assert _ws(1025, 4, 512) == counters(1025) + plist(1025, 512)   # beyond the balanced plan: one CTA per unit
+    assert _ws(1025, 4, 2048) == workspace(1025, 4)
+    # fp32 caches keep the cluster / workspace plan
+    assert _ws(8, 4, 2048, B.BS_FP32) == workspace(8, 4)
+    assert _ws(100, 4, 512, B.BS_FP32) == workspace(100, 4)
+    assert _ws(100, 4, 256, B.BS_FP32) == counters(100) + plist(100, 256)
     limit = 8 << 20
-    assert _ws(124, 4, 2048) <= limit < _ws(125, 4, 2048)
-    assert _ws(62, 8, 2048) <= limit < _ws(63, 8, 2048)
-    assert _ws(124, 4, 512) <= limit < _ws(125, 4, 512) and _ws(303, 4, 512) > limit
-    assert _ws(304, 4, 1024) <= limit and _ws(2044, 4, 1024) <= limit < _ws(2045, 4, 1024)
+    assert _ws(1024, 4, 1024) <= limit
+    assert _ws(746, 8, 1024) <= limit < _ws(747, 8, 1024)
+    assert _ws(708, 4, 2048) <= limit < _ws(709, 4, 2048)
+    assert _ws(500, 8, 2048) <= limit < _ws(501, 8, 2048)
 
 
 class HostCfg:
@@ -222,3 +232,15 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         B.lib()
     with pytest.raises(RuntimeError, match="missing"):
         B.workspace_size(_dims())
+
+
+def test_wait_limit_knob_range():
+    """The device-wait limit takes 1 us .. 60 s and keeps its value on a refused call."""
+    default = B.wait_limit_ns()
+    assert default == 10**9
+    assert B.lib().bs_set_wait_limit_ns(0) == B.BS_ERR_INVALID_ARG
+    assert B.lib().bs_set_wait_limit_ns(61 * 10**9) == B.BS_ERR_INVALID_ARG
+    assert B.wait_limit_ns() == default
+    B.set_wait_limit_ns(5000)
+    assert B.wait_limit_ns() == 5000
+    B.set_wait_limit_ns(default)
