@@ -500,7 +500,8 @@ class Bench:
                 for layer in self.layers:
                     self.layer_calls(layer, i % self.wl.steps)
             self.graphs.append(g)
-        self.launches_per_step = (2 if path == "fused" else 5) * n_layers
+        self.launches_per_layer = bn_launches(path, self.layers[0], B)
+        self.launches_per_step = self.launches_per_layer * n_layers
 
     def _set_parity(self, i):
         for layer in self.layers:
@@ -629,13 +630,12 @@ def run_ours(args) -> None:
     standalone = {k: {"us": round(per_kernel[k], 3),
                       "gbs": round(b0[k] / (per_kernel[k] * 1e-6) / 1e9, 1) if k in ("attn", "score") else None}
                   for k in per_kernel}
-    attn_kernel = "attn_mma_kernel" if wl.dtype == "bf16" else "attn_ffma_kernel"
-    # The roofline of the timed path: one layer step is the front kernel and the attention
-    # launched as its programmatic dependent, overlapping, so the pair is timed as one.
+    # The roofline of the timed path: one layer step is the launches of bs_decode_step,
+    # each a programmatic dependent of the one before (overlapping), timed as one.
     roofline = {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(layer_gbs / peak, 4), "traffic": None,
-                "kernel": (f"bs_decode_step = step_front_kernel + {attn_kernel} (one layer step; the two "
-                           "launches overlap through programmatic dependent launch)" if args.path == "fused"
+                "kernel": (f"bs_decode_step = {step_kernels(wl, bn.launches_per_layer)} (one layer step; "
+                           "the launches overlap through programmatic dependent launch)" if args.path == "fused"
                            else "the five calls of one layer step"),
                 "peak_source": peak_note, "algorithmic_bytes_per_launch": nbytes["layer_step"],
                 "launch_us": round(value, 3),
@@ -707,13 +707,13 @@ def run_ours(args) -> None:
                            "decode_steps_cycled": wl.steps, "kv_dtype": wl.dtype, "q_dtype": wl.dtype,
                            "l2": f"inputs larger than L2: {n_layers} distinct layer buffers per step",
                            "graph": (f"one CUDA graph per decode step, {n_layers} layers x "
-                                     f"{bn_launches(args.path)} launches each"),
+                                     f"{bn.launches_per_layer} launches each"),
                            "ranks": world, "parallelism": f"replicas x{world}, units independent",
                            "path": args.path},
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
-                "gpu_launches": bn_launches(args.path) * n_layers * args.steps, "clocks": clocks,
+                "gpu_launches": bn.launches_per_step * args.steps, "clocks": clocks,
                 "algorithmic_bytes_per_layer": nbytes,
                 "standalone_calls_us_per_launch": standalone,
                 "other_workloads": extras or None,
@@ -724,9 +724,21 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
-def bn_launches(path: str) -> int:
-    """Kernel launches of one layer step: two for bs_decode_step, five for the calls."""
-    return 2 if path == "fused" else 5
+def bn_launches(path: str, layer, B) -> int:
+    """Kernel launches of one layer step: those of one bs_decode_step call (the library
+    says how many for the layer's dims), or five for the separate calls."""
+    if path != "fused":
+        return 5
+    n = B.decode_step_launches(layer.dims)
+    assert n > 0, "bad dims"
+    return n
+
+
+def step_kernels(wl, launches: int) -> str:
+    """The kernels of one bs_decode_step call, in launch order."""
+    attn = "attn_ffma_kernel" if wl.dtype != "bf16" else ("attn_ws_kernel" if launches == 3 else "attn_mma_kernel")
+    front = "step_score_balanced + step_select_kernel" if launches == 3 else "step_front_kernel"
+    return f"{front} + {attn}"
 
 
 def main():

@@ -405,6 +405,10 @@ bs_status bs_lse_merge(const bs_dims *dims, const float *out_a, const float *lse
 /* Bytes of workspace bs_sparse_decode_attn needs for these dims (0 on bad dims). */
 size_t bs_workspace_size(const bs_dims *dims);
 
+/* Kernels one bs_decode_step call launches for these dims (each a programmatic
+ * dependent of the one before), or 0 on bad dims. Host only; launches nothing. */
+int bs_decode_step_launches(const bs_dims *dims);
+
 /* Every wait inside a kernel (for a bulk copy to land, for the fused step's selection
  * to be published) gives up after a wall-clock limit, reports BS_ERR_TIMEOUT in the
  * status word and lets the kernel finish. This sets that limit, in nanoseconds, for the

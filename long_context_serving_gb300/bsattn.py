@@ -110,6 +110,7 @@ _SIGS = {
     "bs_lse_merge": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_workspace_size": (ctypes.c_size_t, [_P(Dims)]),
+    "bs_decode_step_launches": (ctypes.c_int, [_P(Dims)]),
     "bs_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
     "bs_wait_limit_ns": (ctypes.c_uint64, []),
     "bs_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -244,6 +245,11 @@ def lse_merge(dims, out_a, lse_a, out_b, lse_b, out, lse, stream=None):
 
 def workspace_size(dims) -> int:
     return int(lib().bs_workspace_size(ctypes.byref(dims)))
+
+
+def decode_step_launches(dims) -> int:
+    """Kernels one decode_step call launches for these dims (0 on bad dims)."""
+    return int(lib().bs_decode_step_launches(ctypes.byref(dims)))
 
 
 def set_wait_limit_ns(limit_ns: int) -> None:

@@ -114,6 +114,14 @@ size_t bs_workspace_size(const bs_dims *dims) {
   return (head + bsi::attn_record_area_floats(units, G, dims->head_dim, mode)) * sizeof(float);
 }
 
+int bs_decode_step_launches(const bs_dims *dims) {
+  if (bsi::check_dims(dims) != BS_OK) return 0;
+  const int units = dims->batch * dims->n_kv_heads;
+  // Balanced mode: scores, selection, attention; otherwise the front kernel (scores and
+  // selection) and the attention.
+  return bsi::attn_mode(units, dims->max_gather_pages_per_unit, dims->kv_dtype) == bsi::kModeBalanced ? 3 : 2;
+}
+
 bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *c, const int32_t *seq_lens_host) {
   bs_status st = bsi::check_dims(dims);
   if (st != BS_OK) return st;

@@ -669,14 +669,21 @@ __device__ __forceinline__ int select_unit_regs(const SelUnit &su, int32_t *out,
 }
 
 // Selection of one unit into out[0, cap) (and `copy`): the register-resident path up
-// to NT * 32 candidates, otherwise flags and keys in shared memory (keys[n_blk],
-// flags[n_blk]). Returns the count, or -1 when it exceeds cap.
+// to NT * 32 candidates (NT * 8 for CTAs of 1024 threads), otherwise flags and keys in
+// shared memory (keys[n_blk], flags[n_blk]). Returns the count, or -1 when it exceeds
+// cap.
 template <int NT>
 __device__ __forceinline__ int select_unit(const SelUnit &su, uint32_t *keys, uint8_t *flags, int32_t *out, int cap,
                                            int32_t *copy, SelShared<NT> &sh) {
   const int nr = (su.ge.c_hi - su.ge.c_lo + NT - 1) / NT;
   if (nr <= 4) return select_unit_regs<NT, 4>(su, out, cap, copy, sh);
-  if (nr <= 32) return select_unit_regs<NT, 32>(su, out, cap, copy, sh);
+  if (NT >= 1024) {
+    // (1024 threads: registers for up to 8 candidates a thread, the shared-memory path
+    // beyond)
+    if (nr <= 8) return select_unit_regs<NT, (NT >= 1024 ? 8 : 32)>(su, out, cap, copy, sh);
+  } else if (nr <= 32) {
+    return select_unit_regs<NT, (NT >= 1024 ? 8 : 32)>(su, out, cap, copy, sh);
+  }
   select_unit_flags<NT>(su, keys, flags, sh);
   return compact_selection<NT>(flags, su.ge.n_blk, out, cap, copy, sh);
 }
