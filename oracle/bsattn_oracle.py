@@ -20,7 +20,10 @@ What it computes, step by step, in the order and notation of the two method page
    pre-exponential eviction logits under the strict eviction rule) and Gamma_q
    (query-aware top-(k - k_e)) ("Dual-Selection-Mechanismus", "ED-DMA");
 4. softmax attention over only the tokens of the selected blocks (Fluxion,
-   "Probleemstelling" item 1: sparse attention over the selected KV blocks);
+   "Probleemstelling" item 1: sparse attention over the selected KV blocks); and
+   its ED-DMA variant, where each block's pre-exponential eviction logit is added to
+   the logits of its tokens, so its exponential is taken only in the attention
+   (NOSA, "ED-DMA"; a reading, see ed_dma_attention);
 5. the set-difference of the selection against the previous step (NOSA,
    "2. System: NOSI": set-difference kernels for block swapping);
 6. the swap that set-difference drives: the bookkeeping of a GPU block cache holding
@@ -40,11 +43,15 @@ is taken; every such reading is a named argument or constant below:
   Gamma_e; the strict eviction rule applies to Gamma_e's pool only;
 * scale 1/sqrt(d) in both scores and attention.
 
+* ED-DMA in attention: the block's eviction logit is an additive logit bias of
+  each of its tokens (``ed_dma_attention``); plain softmax over the selection stays
+  the default.
+
 Parity unpinned (no page value fixes them; every pin below holds under each
 alternative): the group reduction (max vs mean), the sink/local sizes chosen for
 the synthetic configurations, the rounding of the budget fraction to k, the
-per-block granularity of eviction logits, and ED-DMA's use of the eviction score
-inside attention (not modelled: attention is plain softmax over the selection).
+per-block granularity of eviction logits, and the additive-bias reading of ED-DMA
+itself (its pins fix the formula as read, not the reading).
 """
 
 from __future__ import annotations
@@ -234,6 +241,38 @@ def sparse_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, sel, g: int, T
     return o, lse
 
 
+def ed_dma_attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, sel, g: int, T: int, e_blocks):
+    """Attention of the ED-DMA variant ("Technisches Resümee: NOSA", Methodik /
+    1. Algorithmus: NOSA, ED-DMA: blocks are chosen on the eviction head's
+    pre-exponential logits, and the exponential is applied only in the attention).
+
+    Reading: the pre-exponential eviction logit e[b] of block b enters the softmax as
+    an additive logit of every selected token t of that block, b = t // g:
+        logit_h(t) = q_h.K[t]/sqrt(d) + e[t // g]
+        o_h = sum_t softmax_t(logit_h(t)) V[t],  lse_h = log sum_t exp(logit_h(t)),
+    so exp(e[b]) first appears here, as a factor of the block's attention weights. A
+    block with e[b] = -inf drops out; when no token is left, o_h = 0 and lse_h = -inf.
+    The tokens are those of sparse_attention (selected blocks clipped to t < T).
+    Returns (o [G][d], lse [G])."""
+    G, d = q.shape
+    U = selected_tokens(sel, g, T)
+    e = np.asarray(e_blocks, dtype=np.float64)
+    bias = e[U // g] if U.size else np.zeros(0)
+    keep = bias > -np.inf
+    if not keep.any():
+        return np.zeros((G, d)), np.full(G, -np.inf)
+    U, bias = U[keep], bias[keep]
+    Ku = np.asarray(K[U], dtype=np.float64)
+    Vu = np.asarray(V[U], dtype=np.float64)
+    logits = (np.asarray(q, np.float64) @ Ku.T) / math.sqrt(d) + bias[None, :]   # [G][|U|]
+    m = logits.max(axis=1, keepdims=True)
+    w = np.exp(logits - m)
+    l = w.sum(axis=1)
+    o = (w @ Vu) / l[:, None]
+    lse = m[:, 0] + np.log(l)
+    return o, lse
+
+
 # ---------------------------------------------------------------------------
 # 5. Set-difference against the previous step
 # ---------------------------------------------------------------------------
@@ -328,12 +367,15 @@ def init_state(wl, units=None) -> dict:
     return state
 
 
-def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max", attend_units=None) -> dict:
+def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max", attend_units=None,
+                ed_dma: bool = False) -> dict:
     """Run one decode step for ``units`` (default: all); update ``state`` in place.
 
     ``attend_units``: when given, the attention output (o, lse) is computed only for
     these units and is None for the others; every other result is computed for all
-    ``units``."""
+    ``units``. ``ed_dma``: the attention of every unit is ed_dma_attention with the
+    unit's eviction logits (``wl.evict[u]``) as the block logits; otherwise plain
+    sparse_attention."""
     units = range(wl.U) if units is None else units
     out = {}
     for u in units:
@@ -355,7 +397,10 @@ def decode_step(wl, step: int, state: dict, units=None, group_reduce: str = "max
             st.alive = sel.alive
         o = lse = None
         if attend_units is None or u in attend_units:
-            o, lse = sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
+            if ed_dma:
+                o, lse = ed_dma_attention(q, K, wl.V64(u), sel.sel, g, T, wl.evict[u])
+            else:
+                o, lse = sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
         added, removed = setdiff(st.prev_sel, sel.sel)
         st.prev_sel = list(sel.sel)
         out[u] = UnitStep(T=T, sel=sel, scores=scores, o=o, lse=lse, added=added, removed=removed)

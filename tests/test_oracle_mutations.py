@@ -132,11 +132,37 @@ def _swap_highest_slot_first(slot_block, block_slot, added, removed):
     return sb, bs, copies
 
 
+def _ed_dma_bias_scaled(q, K, V, sel, g, T, e_blocks):
+    return ORIG["ed_dma_attention"](q, K, V, sel, g, T, np.asarray(e_blocks, np.float64) / math.sqrt(q.shape[1]))
+
+
+def _ed_dma_bias_by_position(q, K, V, sel, g, T, e_blocks):
+    e = np.asarray(e_blocks, np.float64)
+    e2 = np.full_like(e, -np.inf)      # block sel[i] takes e[i], the logit of its position
+    for i, c in enumerate(sel):
+        if i < e.size:
+            e2[c] = e[i]
+    return ORIG["ed_dma_attention"](q, K, V, sel, g, T, e2)
+
+
+def _ed_dma_bias_negated(q, K, V, sel, g, T, e_blocks):
+    e = np.asarray(e_blocks, np.float64)
+    return ORIG["ed_dma_attention"](q, K, V, sel, g, T, np.where(np.isneginf(e), e, -e))
+
+
+def _ed_dma_exp_applied_early(q, K, V, sel, g, T, e_blocks):
+    return ORIG["ed_dma_attention"](q, K, V, sel, g, T, np.exp(np.asarray(e_blocks, np.float64)))
+
+
+def _decode_step_ed_dma_ignored(wl, step, state, units=None, group_reduce="max", attend_units=None, ed_dma=False):
+    return ORIG["decode_step"](wl, step, state, units, group_reduce, attend_units)
+
+
 def _decode_step_variant(drop: str):
     """decode_step with one piece of its carried state left out: 'alive' (the eviction
     mask is not carried), 'prev_sel' (the previous selection is not recorded) or 'kbar'
     (the updated summaries are not stored back)."""
-    def step(wl, step_i, state, units=None, group_reduce="max"):
+    def step(wl, step_i, state, units=None, group_reduce="max", attend_units=None, ed_dma=False):
         units = range(wl.U) if units is None else units
         out = {}
         for u in units:
@@ -156,7 +182,12 @@ def _decode_step_variant(drop: str):
                                 scores, evict, st.alive)
             if cls == O.DUAL and drop != "alive":
                 st.alive = sel.alive
-            o, lse = O.sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
+            o = lse = None
+            if attend_units is None or u in attend_units:
+                if ed_dma:
+                    o, lse = O.ed_dma_attention(q, K, wl.V64(u), sel.sel, g, T, wl.evict[u])
+                else:
+                    o, lse = O.sparse_attention(q, K, wl.V64(u), sel.sel, g, T)
             added, removed = O.setdiff(st.prev_sel, sel.sel)
             if drop != "prev_sel":
                 st.prev_sel = list(sel.sel)
@@ -188,6 +219,11 @@ MUTATIONS = {
     "decode_step_alive_not_carried": ("decode_step", _decode_step_variant("alive")),
     "decode_step_prev_sel_not_carried": ("decode_step", _decode_step_variant("prev_sel")),
     "decode_step_kbar_not_stored": ("decode_step", _decode_step_variant("kbar")),
+    "ed_dma_bias_scaled": ("ed_dma_attention", _ed_dma_bias_scaled),
+    "ed_dma_bias_by_position": ("ed_dma_attention", _ed_dma_bias_by_position),
+    "ed_dma_bias_negated": ("ed_dma_attention", _ed_dma_bias_negated),
+    "ed_dma_exp_applied_early": ("ed_dma_attention", _ed_dma_exp_applied_early),
+    "decode_step_ed_dma_ignored": ("decode_step", _decode_step_ed_dma_ignored),
 }
 
 ORIG = {name: getattr(O, name) for name, _ in MUTATIONS.values()}

@@ -463,11 +463,81 @@ def check_p12_decode_step_carry(orc):
             assert crossed, "the dual run must bring new candidates in"
 
 
+# ---------------------------------------------------------------------------
+# ED-DMA attention: the eviction logit of a block as an additive logit of its tokens
+# ("Technisches Resümee: NOSA", Methodik / 1. Algorithmus: NOSA, ED-DMA)
+# ---------------------------------------------------------------------------
+def check_golden_ed_dma(orc):
+    f = _golden.load("ed_dma_bias.txt")
+    o, lse = orc.ed_dma_attention(f["A.q"], f["A.K"], f["A.V"], _golden.ints(f["A.sel"]), _golden.i(f["A.g"]),
+                                  _golden.i(f["A.T"]), f["A.e"])
+    np.testing.assert_allclose(o, f["A.o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, f["A.lse"], rtol=0, atol=1e-12)
+    for c in "BC":
+        q = np.atleast_1d(f[f"{c}.q"])[None, :]
+        K, V = f[f"{c}.K"].reshape(-1, 1), f[f"{c}.V"].reshape(-1, 1)
+        o, lse = orc.ed_dma_attention(q, K, V, _golden.ints(f[f"{c}.sel"]), _golden.i(f[f"{c}.g"]),
+                                      _golden.i(f[f"{c}.T"]), np.atleast_1d(f[f"{c}.e"]))
+        np.testing.assert_allclose(o[0], np.atleast_1d(f[f"{c}.o"]), rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(np.atleast_1d(f[f"{c}.lse"])))
+        fin = np.isfinite(lse)
+        np.testing.assert_allclose(lse[fin], np.atleast_1d(f[f"{c}.lse"])[fin], rtol=0, atol=1e-12)
+
+
+def check_p13_ed_dma(orc):
+    rng = np.random.default_rng(23)
+    for T, g, G, d, n_sel in ((301, 16, 4, 32, 7), (256, 32, 2, 16, 5), (97, 16, 3, 8, 4)):
+        n_blk = -(-T // g)
+        K = rng.standard_normal((T + 5, d))
+        V = rng.standard_normal((T + 5, d))
+        q = rng.standard_normal((G, d))
+        e = rng.standard_normal(n_blk) * 2
+        sel = sorted(set(rng.choice(n_blk - 1, size=n_sel - 1, replace=False).tolist()) | {n_blk - 1})
+        U = np.concatenate([np.arange(c * g, min((c + 1) * g, T)) for c in sel])
+        # The library's attention with the blocks' logits as an additive float mask.
+        o, lse = orc.ed_dma_attention(q, K, V, sel, g, T, e)
+        ref = _sdpa(q, K[U], V[U], (e[U // g]).astype(np.float64))
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+        # lse closes the biased softmax over the selected tokens.
+        logits = (q @ K[U].T) / math.sqrt(d) + e[U // g][None, :]
+        np.testing.assert_allclose(np.exp(logits - lse[:, None]).sum(axis=1), 1.0, rtol=0, atol=1e-12)
+        # A constant logit shifts lse and leaves o alone (plain softmax).
+        o0, lse0 = orc.sparse_attention(q, K, V, sel, g, T)
+        for c in (0.0, -3.5, 7.25):
+            oc, lsec = orc.ed_dma_attention(q, K, V, sel, g, T, np.full(n_blk, c))
+            np.testing.assert_allclose(oc, o0, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lsec, lse0 + c, rtol=0, atol=1e-12)
+        # e = -inf removes a block: the same as not selecting it.
+        drop = sel[len(sel) // 2]
+        e2 = e.copy()
+        e2[drop] = -np.inf
+        o2, lse2 = orc.ed_dma_attention(q, K, V, sel, g, T, e2)
+        o3, lse3 = orc.ed_dma_attention(q, K, V, [c for c in sel if c != drop], g, T, e)
+        np.testing.assert_allclose(o2, o3, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse2, lse3, rtol=0, atol=1e-12)
+    # decode_step(ed_dma=True): the same selections, and every unit's attention is the
+    # library's with that unit's eviction logits as the mask of the selected tokens.
+    wl = make_workload(5, seed=4, B=1, T=1100, steps=2)
+    st_a, st_b = orc.init_state(wl), orc.init_state(wl)
+    for step in range(2):
+        plain = orc.decode_step(wl, step, st_a)
+        ed = orc.decode_step(wl, step, st_b, ed_dma=True)
+        for u in range(wl.U):
+            assert ed[u].sel.sel == plain[u].sel.sel
+            g, T = int(wl.g[u]), ed[u].T
+            U = np.concatenate([np.arange(c * g, min((c + 1) * g, T)) for c in ed[u].sel.sel])
+            mask = np.asarray(wl.evict[u], np.float64)[U // g]
+            ref = _sdpa(wl.q64(step, u), wl.K64(u)[U], wl.V64(u)[U], mask)
+            np.testing.assert_allclose(ed[u].o, ref, rtol=0, atol=1e-10)
+            assert np.abs(ed[u].o - plain[u].o).max() > 1e-6
+
+
 ALL_CHECKS = [check_golden_pooling, check_golden_select_retrieval, check_golden_select_dual,
               check_golden_attention, check_p1_full_budget_is_dense, check_p2_streaming_is_sink_window,
               check_p3_select_brute_force, check_p4_p5_eviction, check_p6_pooling_special_cases,
               check_p7_setdiff, check_p8_planted, check_p9_lse_merge, check_p10_incremental,
-              check_golden_block_swap, check_p11_block_swap_invariants, check_p12_decode_step_carry]
+              check_golden_block_swap, check_p11_block_swap_invariants, check_p12_decode_step_carry,
+              check_golden_ed_dma, check_p13_ed_dma]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
