@@ -669,6 +669,7 @@ def run_ours(args) -> None:
 
     swap = measure_block_swap(layers[0], wl, B, torch) if rank == 0 and not args.no_extras else None
     split = measure_cpu_split(layers[0], wl, B, torch) if rank == 0 and not args.no_extras else None
+    launches_per_layer, launches_per_step = bn.launches_per_layer, bn.launches_per_step
     bn.free()
     del bn, layers
 
@@ -707,13 +708,13 @@ def run_ours(args) -> None:
                            "decode_steps_cycled": wl.steps, "kv_dtype": wl.dtype, "q_dtype": wl.dtype,
                            "l2": f"inputs larger than L2: {n_layers} distinct layer buffers per step",
                            "graph": (f"one CUDA graph per decode step, {n_layers} layers x "
-                                     f"{bn.launches_per_layer} launches each"),
+                                     f"{launches_per_layer} launches each"),
                            "ranks": world, "parallelism": f"replicas x{world}, units independent",
                            "path": args.path},
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h},
-                "gpu_launches": bn.launches_per_step * args.steps, "clocks": clocks,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
                 "algorithmic_bytes_per_layer": nbytes,
                 "standalone_calls_us_per_launch": standalone,
                 "other_workloads": extras or None,

@@ -191,7 +191,15 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * Fluxion, Probleemstelling item 1 (sparse attention over the selected KV blocks)
  * and Kerninzichten item 3 (bound by data movement). For each query head h of unit
  * u, over the tokens U of the selected blocks (each clipped to t < T):
- *   out_h = sum_t softmax_t(q_h . K[t] / sqrt(d)) V[t],  lse_h = log sum_t exp(q_h . K[t] / sqrt(d)).
+ *   out_h = sum_t softmax_t(x_h(t)) V[t],  lse_h = log sum_t exp(x_h(t)),
+ *   x_h(t) = q_h . K[t] / sqrt(d) + e[u][t / g]  (e = 0 when evict_bias is NULL).
+ * evict_bias (device fp32 [units][max_blocks_per_unit], or NULL for plain softmax)
+ * is the ED-DMA variant (NOSA, "ED-DMA": blocks are chosen on the eviction head's
+ * pre-exponential logits and the exponential is applied only in the attention; here
+ * read as each block's logit added to the attention logit of each of its tokens, so
+ * exp(e) weights the block's tokens). Entries must be finite or -inf; a block at -inf
+ * drops out, and a unit whose tokens all drop out gets a zero row and lse = -inf. Only
+ * the entries of selected blocks are read.
  * Split-KV: a unit's gathered pages are cut into contiguous pieces; each piece keeps an
  * fp32 online softmax and the partials are merged by log-sum-exp in a fixed order, so
  * the result does not depend on timing. Three plans, chosen from the dims:
@@ -227,8 +235,9 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * Calls that share a workspace must not run concurrently. */
 bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
                                 const bs_head_cfg *cfg, const int32_t *sel_idx,
-                                const int32_t *sel_cnt, float *out, float *lse, void *workspace,
-                                size_t workspace_bytes, int32_t *dev_status, bs_stream_t stream);
+                                const int32_t *sel_cnt, const float *evict_bias, float *out, float *lse,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                bs_stream_t stream);
 
 /* a4, without a workspace argument. The pages have no counterpart of this call; it
  * exists for callers that cannot allocate device memory for a workspace: a plugin
@@ -255,8 +264,8 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * library routine. */
 bs_status bs_sparse_decode_attn_noalloc(const bs_dims *dims, const void *q, const bs_kv *kv,
                                         const bs_head_cfg *cfg, const int32_t *sel_idx,
-                                        const int32_t *sel_cnt, float *out, float *lse,
-                                        int32_t *dev_status, bs_stream_t stream);
+                                        const int32_t *sel_cnt, const float *evict_bias, float *out,
+                                        float *lse, int32_t *dev_status, bs_stream_t stream);
 
 /* a5. Set-difference of selections.
  * NOSA, "2. System: NOSI": set-difference kernels drive block swapping.
@@ -275,6 +284,8 @@ typedef struct {
   float *scores;              /* [units][max_blocks_per_unit] scratch: this step's candidate scores */
   const float *evict_logits;  /* [units][max_blocks_per_unit]; may be NULL when no unit is DUAL */
   uint8_t *alive;             /* [units][max_blocks_per_unit], in/out; may be NULL when no unit is DUAL */
+  const float *evict_bias;    /* the attention's ED-DMA block logits, as for bs_sparse_decode_attn (NULL:
+                                 plain softmax); may be evict_logits itself */
   const int32_t *prev_idx, *prev_cnt;  /* previous step's selection (prev_cnt 0 at the first step) */
   int32_t *cur_idx, *cur_cnt;          /* this step's selection (written); must not alias prev */
   int32_t *added, *added_cnt, *removed, *removed_cnt;  /* set-difference (written) */
@@ -380,6 +391,9 @@ typedef struct {
   const int32_t *page_table;    /* [units][max_pages_per_unit]: host page of each logical page */
   const int32_t *seq_lens;      /* [batch]: T */
   const int32_t *block_tokens;  /* [units]: g */
+  const float *evict_bias;      /* NULL, or the ED-DMA block logits [units][max_blocks_per_unit] as for
+                                   bs_sparse_decode_attn */
+  int32_t max_blocks_per_unit;  /* row length of evict_bias (used only when it is set) */
 } bs_host_tables;
 
 /* Attention of each unit's listed blocks (tokens clipped to T) on the host cores,

@@ -53,7 +53,8 @@ class HeadCfg(ctypes.Structure):
 
 class StepIO(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("summaries", ctypes.c_void_p), ("scores", ctypes.c_void_p),
-                ("evict_logits", ctypes.c_void_p), ("alive", ctypes.c_void_p), ("prev_idx", ctypes.c_void_p),
+                ("evict_logits", ctypes.c_void_p), ("alive", ctypes.c_void_p), ("evict_bias", ctypes.c_void_p),
+                ("prev_idx", ctypes.c_void_p),
                 ("prev_cnt", ctypes.c_void_p), ("cur_idx", ctypes.c_void_p), ("cur_cnt", ctypes.c_void_p),
                 ("added", ctypes.c_void_p), ("added_cnt", ctypes.c_void_p), ("removed", ctypes.c_void_p),
                 ("removed_cnt", ctypes.c_void_p), ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
@@ -73,7 +74,8 @@ class BlockCache(ctypes.Structure):
 
 
 class HostTables(ctypes.Structure):
-    _fields_ = [("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("block_tokens", ctypes.c_void_p)]
+    _fields_ = [("page_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p), ("block_tokens", ctypes.c_void_p),
+                ("evict_bias", ctypes.c_void_p), ("max_blocks_per_unit", ctypes.c_int32)]
 
 
 class BsError(RuntimeError):
@@ -94,13 +96,14 @@ _SIGS = {
                                       ctypes.c_void_p]),
     "bs_sparse_decode_attn": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, _P(KV), _P(HeadCfg), ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                             ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+                                             ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_block_setdiff": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "bs_sparse_decode_attn_noalloc": (ctypes.c_int, [_P(Dims), ctypes.c_void_p, _P(KV), _P(HeadCfg),
                                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+                                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                     ctypes.c_void_p]),
     "bs_decode_step": (ctypes.c_int, [_P(Dims), _P(KV), _P(HeadCfg), _P(StepIO), ctypes.c_int, ctypes.c_void_p]),
     "bs_block_swap": (ctypes.c_int, [_P(Dims), _P(HeadCfg), ctypes.c_void_p, _P(HostKV), _P(BlockCache),
                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -190,12 +193,15 @@ def select_topk(dims, cfg, seq_lens, scores, evict_logits, alive, sel_idx, sel_c
                                 _stream(stream)))
 
 
-def sparse_decode_attn(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, workspace, dev_status, stream=None):
+def sparse_decode_attn(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, workspace, dev_status, stream=None,
+                       evict_bias=None):
+    """a4. evict_bias (None: plain softmax) is the ED-DMA logit bias of every block,
+    fp32 [units][max_blocks_per_unit] on the device."""
     nbytes = workspace.numel() * workspace.element_size()
     _check("bs_sparse_decode_attn",
            lib().bs_sparse_decode_attn(ctypes.byref(dims), _ptr(q), ctypes.byref(kv), ctypes.byref(cfg),
-                                       _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse), _ptr(workspace),
-                                       nbytes, _ptr(dev_status), _stream(stream)))
+                                       _ptr(sel_idx), _ptr(sel_cnt), _ptr(evict_bias), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), nbytes, _ptr(dev_status), _stream(stream)))
 
 
 def block_setdiff(dims, prev_idx, prev_cnt, cur_idx, cur_cnt, added, added_cnt, removed, removed_cnt, dev_status,
@@ -206,13 +212,14 @@ def block_setdiff(dims, prev_idx, prev_cnt, cur_idx, cur_cnt, added, added_cnt, 
                                   _stream(stream)))
 
 
-def sparse_decode_attn_noalloc(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, dev_status, stream=None):
+def sparse_decode_attn_noalloc(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, dev_status, stream=None,
+                               evict_bias=None):
     """bs_sparse_decode_attn for callers that cannot allocate a workspace: the library's
     fixed per-device scratch array stands in for it (see include/bsattn.h)."""
     _check("bs_sparse_decode_attn_noalloc",
            lib().bs_sparse_decode_attn_noalloc(ctypes.byref(dims), _ptr(q), ctypes.byref(kv), ctypes.byref(cfg),
-                                               _ptr(sel_idx), _ptr(sel_cnt), _ptr(out), _ptr(lse),
-                                               _ptr(dev_status), _stream(stream)))
+                                               _ptr(sel_idx), _ptr(sel_cnt), _ptr(evict_bias), _ptr(out),
+                                               _ptr(lse), _ptr(dev_status), _stream(stream)))
 
 
 def decode_step(dims, kv, cfg, io: StepIO, group_reduce=BS_GROUP_MAX, stream=None):

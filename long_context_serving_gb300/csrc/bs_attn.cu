@@ -7,8 +7,8 @@ namespace bsi {
 namespace {
 
 bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv, const bs_head_cfg *cfg,
-                            const int32_t *sel_idx, const int32_t *sel_cnt, float *out, float *lse, float *ws,
-                            int32_t *st, cudaStream_t cs) {
+                            const int32_t *sel_idx, const int32_t *sel_cnt, const float *bias, float *out,
+                            float *lse, float *ws, int32_t *st, cudaStream_t cs) {
   const int units = dims->batch * dims->n_kv_heads;
   AttnArgs a;
   a.dims = *dims;
@@ -17,6 +17,7 @@ bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv,
   a.cfg = *cfg;
   a.sel_idx = sel_idx;
   a.sel_cnt = sel_cnt;
+  a.bias = bias;
   a.out = out;
   a.lse = lse;
   const StepWords w = step_words(ws, units);
@@ -36,8 +37,8 @@ bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv,
 
 extern "C" bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
                                            const bs_head_cfg *cfg, const int32_t *sel_idx, const int32_t *sel_cnt,
-                                           float *out, float *lse, void *workspace, size_t workspace_bytes,
-                                           int32_t *dev_status, bs_stream_t stream) {
+                                           const float *evict_bias, float *out, float *lse, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_status, bs_stream_t stream) {
   using namespace bsi;
   bs_status s = check_dims(dims);
   if (s != BS_OK) return s;
@@ -48,8 +49,8 @@ extern "C" bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, c
       !aligned16(workspace))
     return BS_ERR_ALIGN;
   if (workspace_bytes < bs_workspace_size(dims)) return BS_ERR_CAPACITY;
-  return launch_standalone(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, static_cast<float *>(workspace),
-                           dev_status, reinterpret_cast<cudaStream_t>(stream));
+  return launch_standalone(dims, q, kv, cfg, sel_idx, sel_cnt, evict_bias, out, lse,
+                           static_cast<float *>(workspace), dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -95,8 +96,8 @@ bs_status fixed_scratch_address(void **addr) {
 
 extern "C" bs_status bs_sparse_decode_attn_noalloc(const bs_dims *dims, const void *q, const bs_kv *kv,
                                                    const bs_head_cfg *cfg, const int32_t *sel_idx,
-                                                   const int32_t *sel_cnt, float *out, float *lse,
-                                                   int32_t *dev_status, bs_stream_t stream) {
+                                                   const int32_t *sel_cnt, const float *evict_bias, float *out,
+                                                   float *lse, int32_t *dev_status, bs_stream_t stream) {
   using namespace bsi;
   bs_status s = check_dims(dims);
   if (s != BS_OK) return s;
@@ -114,6 +115,6 @@ extern "C" bs_status bs_sparse_decode_attn_noalloc(const bs_dims *dims, const vo
   // call (possibly one that stopped early) left in it.
   const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
   if (cudaMemsetAsync(scratch, 0, attn_counter_floats(units) * sizeof(float), cs) != cudaSuccess) return BS_ERR_CUDA;
-  return launch_standalone(dims, q, kv, cfg, sel_idx, sel_cnt, out, lse, static_cast<float *>(scratch), dev_status,
-                           cs);
+  return launch_standalone(dims, q, kv, cfg, sel_idx, sel_cnt, evict_bias, out, lse, static_cast<float *>(scratch),
+                           dev_status, cs);
 }

@@ -208,10 +208,12 @@ __device__ UnitBlocks load_unit_blocks(const AttnArgs &a, int u, int32_t *sel_sm
 }
 
 // Resolves page slot `lane` (< kStagePages) of a stage: returns the physical page and
-// the number of valid tokens in it (0 for an empty or out-of-range slot).
+// the number of valid tokens in it (0 for an empty or out-of-range slot). blk_out (may
+// be null) receives the page's block index, -1 for an empty slot.
 __device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims &dims, const int32_t *pt, int gp,
-                                            int gp1, int *phys_out, int32_t *st) {
+                                            int gp1, int *phys_out, int *blk_out, int32_t *st) {
   *phys_out = -1;
+  if (blk_out) *blk_out = -1;
   if (gp >= gp1) return 0;
   if (ub.plist) {
     // Pages come resolved; all are full but the unit's last, which holds token T-1.
@@ -221,11 +223,13 @@ __device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims 
       return 0;
     }
     *phys_out = phys;
+    if (blk_out) *blk_out = __ldcg(ub.sel + gp / (ub.g / kPage));
     return gp == ub.pg.n_pages - 1 ? (ub.T - 1) % kPage + 1 : kPage;
   }
   const int ppb = ub.pg.ppb;
   const int i = gp / ppb, pb = gp - i * ppb;
   const int c = ub.block(i);
+  if (blk_out) *blk_out = c;
   const int lp = c * ppb + pb;
   const int t0 = lp * kPage;
   if (c < 0 || lp >= dims.max_pages_per_unit || t0 >= ub.T) {
@@ -239,6 +243,18 @@ __device__ __forceinline__ int resolve_page(const UnitBlocks &ub, const bs_dims 
   }
   *phys_out = phys;
   return min(kPage, ub.T - t0);
+}
+
+// The logit bias of block c of unit u in log2 units: 0 without biases (or for an empty
+// slot), else log2(e) * bias[u][c] (a block index outside the row reports
+// BS_ERR_DEVICE_BOUNDS and drops the page).
+__device__ __forceinline__ float block_bias2(const float *bias, const bs_dims &dims, int u, int c, int32_t *st) {
+  if (bias == nullptr || c < 0) return 0.0f;
+  if (c >= dims.max_blocks_per_unit) {
+    report(st, BS_ERR_DEVICE_BOUNDS);
+    return -INFINITY;
+  }
+  return __ldg(bias + static_cast<size_t>(u) * dims.max_blocks_per_unit + c) * kLog2e;
 }
 
 // Output row of one head from an unnormalised state (o, m in log2 units, l): o / l and
@@ -550,12 +566,14 @@ __device__ __forceinline__ void load_q_frags(const void *q, size_t orow0, bool q
 // m_run[], l_run[] (log2 units; replicated over the 8 lanes with equal lane%4) and
 // o[m][j] = O[head h(j)][dim 16m + lane/4 + 8 (j >> 1)], j = (j & 1) picking the head.
 // `valid` tokens (1..16) hold data: rows past it are zeroed in V and masked out of S.
-// Scores in log2 units (qk_scale = log2(e) / sqrt(d)). Called by all 32 lanes.
+// Scores in log2 units (qk_scale = log2(e) / sqrt(d)); bias2 (log2 units) is added to
+// the score of every token of the page (0 for plain attention, -inf drops the page).
+// Called by all 32 lanes.
 template <int D>
 __device__ __forceinline__ void mma_page(unsigned char *kpg, unsigned char *vpg, int valid,
                                          const uint32_t (&qa_hi)[D / 16][2], const uint32_t (&qa_lo)[D / 16][2],
-                                         bool q32, float qk_scale, float (&m_run)[2], float (&l_run)[2],
-                                         float (&o)[D / 16][4]) {
+                                         bool q32, float qk_scale, float bias2, float (&m_run)[2],
+                                         float (&l_run)[2], float (&o)[D / 16][4]) {
   constexpr int KSTEPS = D / 16;
   const int lane = threadIdx.x & 31;
   if (valid < kPage) {
@@ -587,7 +605,7 @@ __device__ __forceinline__ void mma_page(unsigned char *kpg, unsigned char *vpg,
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int t = t0 + 8 * (j >> 1);
-    x[j] = t < valid ? (s0[j] + s1[j]) * qk_scale : -INFINITY;
+    x[j] = t < valid ? (s0[j] + s1[j]) * qk_scale + bias2 : -INFINITY;
   }
   float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
@@ -682,6 +700,7 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   constexpr int R = L::kRing;
   __shared__ uint64_t bars[R];
   __shared__ int slot_valid[R][kStagePages];
+  __shared__ float slot_bias[R][kStagePages];   // log2 units, 0 without biases
   const bs_dims &dims = a.dims;
   int32_t *st = a.st;
 
@@ -713,15 +732,19 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   // one round of page-table loads per chunk) and starts the copies of a stage's 4
   // pages (one TMA box per 64-column half of a page, for K and for V).
   int chunk = -1, ch_phys = -1, ch_valid = 0;
+  float ch_bias = 0.0f;
   auto issue = [&](int stage, int buf) {
     const int first = stage * kStagePages;  // stages never straddle a chunk
     if (first / 32 != chunk) {
       chunk = first / 32;
-      ch_valid = resolve_page(ub, dims, pt, gp0 + chunk * 32 + lane, gp1, &ch_phys, st);
+      int blk = -1;
+      ch_valid = resolve_page(ub, dims, pt, gp0 + chunk * 32 + lane, gp1, &ch_phys, a.bias ? &blk : nullptr, st);
+      ch_bias = block_bias2(a.bias, dims, u, blk, st);
     }
     const int src = first - chunk * 32 + (lane & (kStagePages - 1));
     const int phys_l = __shfl_sync(0xffffffffu, ch_phys, src);
     const int valid_l = __shfl_sync(0xffffffffu, ch_valid, src);
+    const float bias_l = __shfl_sync(0xffffffffu, ch_bias, src);
     const int phys = lane < kStagePages ? phys_l : -1;
     const int valid_tok = lane < kStagePages ? valid_l : 0;
     const unsigned m = __ballot_sync(0xffffffffu, valid_tok > 0);
@@ -737,7 +760,10 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
         tma_load_2d(vdst + hh * L::kHalfBytes, tmv, hh * 64, phys * kPage, &bars[buf]);
       }
     }
-    if (lane < kStagePages) slot_valid[buf][lane] = valid_tok;
+    if (lane < kStagePages) {
+      slot_valid[buf][lane] = valid_tok;
+      slot_bias[buf][lane] = bias_l;
+    }
   };
   if (warp == 0)
     for (int i = 0; i < R && i < n_stages; ++i) issue(i, i);
@@ -767,7 +793,8 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
     const int valid = slot_valid[buf][warp];
     if (valid > 0) {
       unsigned char *kpg = smem + buf * L::kBufBytes + warp * L::kPageBytes;
-      mma_page<D>(kpg, kpg + L::kStageKV, valid, qa_hi, qa_lo, q32, qk_scale, m_run, l_run, o);
+      mma_page<D>(kpg, kpg + L::kStageKV, valid, qa_hi, qa_lo, q32, qk_scale, slot_bias[buf][warp], m_run, l_run,
+                  o);
     }
     __syncthreads();
     if (warp == 0 && it + R < n_stages) issue(it + R, buf);
@@ -863,6 +890,7 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
   constexpr int kPer = D / 16;  // 16-byte chunks per quarter of a row (fp32: D/4 chunks per row)
   __shared__ uint64_t bars[2];
   __shared__ int slot_valid[2][kStagePages];
+  __shared__ float slot_bias[2][kStagePages];   // log2 units, 0 without biases
   __shared__ float ml_sm[2][kMaxG];
 
   const int u = blockIdx.y, split = blockIdx.x;
@@ -895,8 +923,10 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
   __syncthreads();
 
   auto issue = [&](int stage, int buf) {
-    int phys = -1, valid_tok = 0;
-    if (lane < kStagePages) valid_tok = resolve_page(ub, dims, pt, gp0 + stage * kStagePages + lane, gp1, &phys, st);
+    int phys = -1, valid_tok = 0, blk = -1;
+    if (lane < kStagePages)
+      valid_tok = resolve_page(ub, dims, pt, gp0 + stage * kStagePages + lane, gp1, &phys, a.bias ? &blk : nullptr, st);
+    const float bias2 = lane < kStagePages ? block_bias2(a.bias, dims, u, blk, st) : 0.0f;
     const unsigned m = __ballot_sync(0xffffffffu, valid_tok > 0);
     if (lane == 0) mbar_arrive_expect_tx(&bars[buf], static_cast<uint32_t>(__popc(m)) * 2u * L::kPageBytes);
     __syncwarp();
@@ -906,7 +936,10 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
       bulk_g2s(smem + buf * L::kStageBytes + lane * L::kPageBytes, kpool + src, L::kPageBytes, &bars[buf]);
       bulk_g2s(smem + (2 + buf) * L::kStageBytes + lane * L::kPageBytes, vpool + src, L::kPageBytes, &bars[buf]);
     }
-    if (lane < kStagePages) slot_valid[buf][lane] = valid_tok;
+    if (lane < kStagePages) {
+      slot_valid[buf][lane] = valid_tok;
+      slot_bias[buf][lane] = bias2;
+    }
   };
 
   if (warp == 0) {
@@ -964,7 +997,7 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
     }
 #pragma unroll
     for (int h = 0; h < G; ++h)
-      if ((h & 3) == qq) s_sm[h * kStageTokens + tok] = tvalid ? a[h] : -INFINITY;
+      if ((h & 3) == qq) s_sm[h * kStageTokens + tok] = tvalid ? a[h] + slot_bias[buf][tok >> 4] : -INFINITY;
     __syncthreads();
 
     if (warp < G) {

@@ -13,6 +13,7 @@ struct AttnArgs {
   bs_head_cfg cfg;
   const int32_t *sel_idx;
   const int32_t *sel_cnt;
+  const float *bias;  // logit bias of every block [units][max_blocks_per_unit] (ED-DMA), or null
   float *out;
   float *lse;
   int32_t *arrivals;  // per-unit arrival tickets of the splits (workspace and balanced modes)

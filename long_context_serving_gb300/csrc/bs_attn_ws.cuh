@@ -49,7 +49,8 @@ struct WsLayout {
   static constexpr int kMergeBatch = 64;                        // records merged per pass
   static constexpr int kOffPages = kOffScratch + 2 * kMaxG * kMergeBatch * 4;  // resolved pages [kPageWin]
   static constexpr int kPageWin = 256;                          // pages resolved per round
-  static constexpr int kBytes = kOffPages + kPageWin * 4;       // two CTAs per SM
+  static constexpr int kOffBias = kOffPages + kPageWin * 4;     // their logit biases [kPageWin]
+  static constexpr int kBytes = kOffBias + kPageWin * 4;        // two CTAs per SM
 };
 
 // A resolved page: physical page | ((valid tokens - 1) << 27), non-negative since pools
@@ -159,6 +160,7 @@ template <int NS>
 struct WsShared {
   uint64_t full_bar[NS], empty_bar[NS];
   int slot_valid[NS];
+  float slot_bias[NS];   // log2 units, 0 without biases
   int scan_tmp[kWsThreads / 32];
   int is_last, abort_flag;
   float mfin[kMaxG], lfin[kMaxG], wfin[kWsConsumers][kMaxG];
@@ -289,8 +291,10 @@ __device__ __noinline__ void ws_producer(const AttnArgs &a, const CUtensorMap *t
   const int U = pl.U, p0 = pl.p0, p1 = pl.p1;
   uint64_t *full_bar = sh.full_bar, *empty_bar = sh.empty_bar;
   int *slot_valid = sh.slot_valid;
+  float *slot_bias = sh.slot_bias;
   {
     int *pages = reinterpret_cast<int *>(smem + L::kOffPages);
+    float *pbias = reinterpret_cast<float *>(smem + L::kOffBias);
     int last_use[NS];           // use index of each slot's latest page (-1: none)
 #pragma unroll
     for (int i = 0; i < NS; ++i) last_use[i] = -1;
@@ -342,6 +346,18 @@ __device__ __noinline__ void ws_producer(const AttnArgs &a, const CUtensorMap *t
             }
           }
         }
+        if (a.bias != nullptr) {
+          // The block of each page (from the selection when the pages came resolved)
+          // and its logit bias.
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int lp = w0 + lane + 32 * r;
+            if (lp >= w1) continue;
+            int c = -1;
+            if (lp < n_act) c = plist != nullptr ? __ldcg(sel + lp / ppb) : blk[r];
+            pbias[lp - w0] = block_bias2(a.bias, dims, u, c, st);
+          }
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
           const int lp = w0 + lane + 32 * r;
@@ -381,6 +397,7 @@ __device__ __noinline__ void ws_producer(const AttnArgs &a, const CUtensorMap *t
             const int e = pages[lp - w0];
             const int valid = e < 0 ? 0 : (e >> 27) + 1, phys = e & ((1 << 27) - 1);
             slot_valid[slot] = valid;
+            slot_bias[slot] = a.bias != nullptr ? pbias[lp - w0] : 0.0f;
             last_use[slot] = use;
             mbar_arrive_expect_tx(&full_bar[slot], valid > 0 ? 2u * L::kPageBytes : 0u);
             if (valid > 0) {
@@ -562,7 +579,8 @@ __device__ __noinline__ void ws_consumer(const AttnArgs &a, unsigned char *smem,
       const int valid = ok ? slot_valid[slot] : 0;
       if (valid > 0) {
         unsigned char *kpg = smem + slot * L::kSlotBytes;
-        mma_page<D>(kpg, kpg + L::kPageBytes, valid, qa_hi, qa_lo, q32, qk_scale, m_run, l_run, o);
+        mma_page<D>(kpg, kpg + L::kPageBytes, valid, qa_hi, qa_lo, q32, qk_scale, sh.slot_bias[slot], m_run, l_run,
+                    o);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[slot]);

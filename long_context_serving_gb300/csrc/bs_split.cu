@@ -52,6 +52,16 @@ bool cpu_unit(const bs_dims &d, const void *q, const bs_host_tables &t, const vo
       ok = false;
       continue;
     }
+    // ED-DMA: the block's logit is added to each of its tokens' logits; -inf drops it.
+    float eb = 0.0f;
+    if (t.evict_bias != nullptr) {
+      if (c >= t.max_blocks_per_unit) {
+        ok = false;
+        continue;
+      }
+      eb = t.evict_bias[static_cast<size_t>(u) * t.max_blocks_per_unit + c];
+      if (eb == -INFINITY) continue;
+    }
     const int t1 = std::min(T, (c + 1) * g);
     for (int tok = c * g; tok < t1; ++tok) {
       const int lp = tok / kPage;
@@ -72,7 +82,7 @@ bool cpu_unit(const bs_dims &d, const void *q, const bs_host_tables &t, const vo
       for (int h = 0; h < G; ++h) {
         float acc = 0.0f;
         for (int i = 0; i < D; ++i) acc = fmaf(qs[h * D + i], k[i], acc);
-        s[h] = acc;
+        s[h] = acc + eb;
       }
       for (int h = 0; h < G; ++h) {
         const float mn = std::max(m[h], s[h]);
@@ -128,7 +138,8 @@ extern "C" bs_status bs_cpu_sparse_attn(const bs_dims *dims, const void *q, cons
   bs_status s = check_dims(dims);
   if (s != BS_OK) return s;
   if (!q || !kv || !kv->k_pool || !kv->v_pool || !tables || !tables->page_table || !tables->seq_lens ||
-      !tables->block_tokens || !sel_idx || !sel_cnt || !out || !lse || kv->n_pages < 1)
+      !tables->block_tokens || !sel_idx || !sel_cnt || !out || !lse || kv->n_pages < 1 ||
+      (tables->evict_bias != nullptr && tables->max_blocks_per_unit < 1))
     return BS_ERR_INVALID_ARG;
   const int units = dims->batch * dims->n_kv_heads;
   const int nt = std::max(1, std::min(n_threads, units));

@@ -678,6 +678,7 @@ bs_status launch_step_attention(const bs_dims &dims, const bs_kv &kv, const bs_h
   a.cfg = cfg;
   a.sel_idx = io.cur_idx;
   a.sel_cnt = io.cur_cnt;
+  a.bias = io.evict_bias;
   a.out = io.out;
   a.lse = io.lse;
   a.arrivals = words.arrivals;

@@ -36,8 +36,10 @@ class PagedLayer:
     ``q_fp32``: pass the queries as fp32 (the same values, widened) over a bf16 cache.
     """
 
-    def __init__(self, wl, device="cuda", fill=float("nan"), preload_all=False, q_fp32=False):
+    def __init__(self, wl, device="cuda", fill=float("nan"), preload_all=False, q_fp32=False, ed_dma=False):
         self.wl = wl
+        # ED-DMA attention: the eviction logits also enter the attention as block logits.
+        self.ed_dma = bool(ed_dma)
         self.device = torch.device(device)
         U, d, G = wl.U, wl.d, wl.G
         T_cap = wl.T_cap
@@ -109,6 +111,8 @@ class PagedLayer:
             ev[:, :wl.evict.shape[1]] = wl.evict[:, :MB]
             self.evict = torch.as_tensor(ev, device=dev)
             self.alive = torch.ones((U, MB), dtype=torch.uint8, device=dev)
+        if self.ed_dma and self.evict is None:
+            raise ValueError("ED-DMA attention needs a workload with eviction logits")
         self.sel = [torch.full((U, MS), -1, dtype=torch.int32, device=dev) for _ in range(2)]
         self.cnt = [torch.zeros(U, dtype=torch.int32, device=dev) for _ in range(2)]
         self.cur = 0                                         # index of the buffer the next select writes
@@ -167,7 +171,8 @@ class PagedLayer:
 
     def attend(self, step: int, stream=None) -> None:
         B.sparse_decode_attn(self.dims, self.q[step], self.kv_at(self.seq_lens[step]), self.cfg, self.sel[self.cur],
-                             self.cnt[self.cur], self.out, self.lse, self.workspace, self.status, stream)
+                             self.cnt[self.cur], self.out, self.lse, self.workspace, self.status, stream,
+                             evict_bias=self.evict if self.ed_dma else None)
 
     def setdiff(self, stream=None) -> None:
         prev = 1 - self.cur
@@ -180,6 +185,7 @@ class PagedLayer:
         ptr = lambda t: 0 if t is None else t.data_ptr()  # noqa: E731
         return B.StepIO(q=self.q[step].data_ptr(), summaries=self.summaries.data_ptr(),
                         scores=self.scores.data_ptr(), evict_logits=ptr(self.evict), alive=ptr(self.alive),
+                        evict_bias=ptr(self.evict) if self.ed_dma else 0,
                         prev_idx=self.sel[prev].data_ptr(), prev_cnt=self.cnt[prev].data_ptr(),
                         cur_idx=self.sel[self.cur].data_ptr(), cur_cnt=self.cnt[self.cur].data_ptr(),
                         added=self.added.data_ptr(), added_cnt=self.added_cnt.data_ptr(),

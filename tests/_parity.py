@@ -75,7 +75,7 @@ def attention_errors(o_gpu: np.ndarray, o_ref: np.ndarray):
 
 
 def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_sample=None, seed=0,
-               fused=False, q_fp32=False, attend_units=None) -> Report:
+               fused=False, q_fp32=False, attend_units=None, ed_dma=False) -> Report:
     """Drive the GPU path and the oracle through the same steps on ``units`` (default all).
 
     ``attend_units``: compare the attention output only on these units (the oracle's
@@ -83,6 +83,8 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
     alive masks and set-differences are compared on every unit of ``units``.
 
     ``q_fp32``: queries passed as fp32 (the same values) over the bf16 cache.
+    ``ed_dma``: the attention adds each block's eviction logit to its tokens' logits
+    (oracle: ed_dma_attention) on both sides.
     ``fused``: run each step through bs_decode_step (one call for all five steps). A
     near-tie unit whose GPU selection differs from the oracle's then cannot be given
     the oracle's selection before attention: its attention and set-difference are not
@@ -91,7 +93,7 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
     units = list(range(wl.U)) if units is None else list(units)
     reduce_code = B.BS_GROUP_MAX if group_reduce == "max" else B.BS_GROUP_MEAN
     rng = np.random.default_rng(seed)
-    layer = PagedLayer(wl, q_fp32=q_fp32)
+    layer = PagedLayer(wl, q_fp32=q_fp32, ed_dma=ed_dma)
     layer.prefill()
     state = O.init_state(wl, units)
     rep = Report()
@@ -108,7 +110,7 @@ def run_parity(wl, units=None, group_reduce="max", steps=None, summary_rows_samp
             sel_buf = layer.cur
         torch.cuda.synchronize()
         alive_before = {u: None if state[u].alive is None else state[u].alive.copy() for u in units}
-        res = O.decode_step(wl, step, state, units, group_reduce, attend_units=attend_units)
+        res = O.decode_step(wl, step, state, units, group_reduce, attend_units=attend_units, ed_dma=ed_dma)
         gsel = layer.selection(sel_buf)
         scores = layer.scores.cpu().numpy()
         alive = layer.alive.cpu().numpy() if layer.alive is not None else None

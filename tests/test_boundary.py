@@ -58,10 +58,10 @@ def test_pool_rows_stay_below_two_to_the_31():
     kv = B.KV(k_pool=0x10000, v_pool=0x20000, page_table=0x30000, seq_lens=0x40000)
     cfg = B.HeadCfg(*([0x50000] * 9))
     ref = ctypes.byref
-    assert L.bs_sparse_decode_attn(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+    assert L.bs_sparse_decode_attn(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, None, 0x4000, 0x5000, 0x8000,
                                    1 << 30, 0x6000, None) == B.BS_ERR_CAPACITY
-    assert L.bs_sparse_decode_attn_noalloc(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000,
-                                           0x6000, None) == B.BS_ERR_CAPACITY
+    assert L.bs_sparse_decode_attn_noalloc(ref(big), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, None, 0x4000,
+                                           0x5000, 0x6000, None) == B.BS_ERR_CAPACITY
     assert L.bs_build_block_summaries(ref(big), ref(kv), ref(cfg), 0x1000, 1, 0x70000, 0x6000, None) == \
         B.BS_ERR_CAPACITY
 
@@ -160,7 +160,7 @@ def test_calls_reject_bad_arguments_before_launch():
     assert L.bs_score_blocks(ref(d), None, ref(cfg), 0x1000, 0x2000, 0, 0x3000, st, None) == B.BS_ERR_INVALID_ARG
     assert L.bs_select_topk(ref(d), ref(cfg), None, 0x1000, None, None, 0x2000, 0x3000, st, None) == \
         B.BS_ERR_INVALID_ARG
-    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, None,
+    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, None, 0x4000, 0x5000, None,
                                    1 << 30, st, None) == B.BS_ERR_INVALID_ARG
     assert L.bs_block_setdiff(ref(d), 0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, st,
                               None) == B.BS_ERR_INVALID_ARG
@@ -171,7 +171,7 @@ def test_calls_reject_bad_arguments_before_launch():
     assert L.bs_select_topk(ref(_dims(n_q_heads=20)), ref(cfg), 0x1000, 0x1000, None, None, 0x2000, 0x3000, st,
                             None) == B.BS_ERR_SHAPE
     # misaligned pointers
-    assert L.bs_sparse_decode_attn(ref(d), 0x1002, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+    assert L.bs_sparse_decode_attn(ref(d), 0x1002, ref(kv), ref(cfg), 0x2000, 0x3000, None, 0x4000, 0x5000, 0x8000,
                                    1 << 30, st, None) == B.BS_ERR_ALIGN
     bad_kv = B.KV(k_pool=0x10008, v_pool=0x20000, page_table=0x30000, seq_lens=0x40000)
     assert L.bs_build_block_summaries(ref(d), ref(bad_kv), ref(cfg), 0x1000, 1, 0x70000, st, None) == B.BS_ERR_ALIGN
@@ -181,7 +181,7 @@ def test_calls_reject_bad_arguments_before_launch():
     assert L.bs_build_block_summaries(ref(d), ref(kv), ref(cfg), 0x1000, 0, 0x70000, st, None) == \
         B.BS_ERR_INVALID_ARG
     # workspace too small
-    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, 0x4000, 0x5000, 0x8000,
+    assert L.bs_sparse_decode_attn(ref(d), 0x1000, ref(kv), ref(cfg), 0x2000, 0x3000, None, 0x4000, 0x5000, 0x8000,
                                    16, st, None) == B.BS_ERR_CAPACITY
 
 
@@ -218,6 +218,10 @@ def test_offload_and_split_calls_reject_bad_arguments():
     assert L.bs_cpu_sparse_attn(ref(d), 0x1000, ref(host), ref(B.HostTables(page_table=0, seq_lens=0x2000,
                                                                            block_tokens=0x3000)),
                                 0x4000, 0x5000, 0x6000, 0x7000, 4) == B.BS_ERR_INVALID_ARG
+    no_row = B.HostTables(page_table=0x1000, seq_lens=0x2000, block_tokens=0x3000, evict_bias=0x8000,
+                          max_blocks_per_unit=0)   # block logits without a row length
+    assert L.bs_cpu_sparse_attn(ref(d), 0x1000, ref(host), ref(no_row), 0x4000, 0x5000, 0x6000, 0x7000, 4) == \
+        B.BS_ERR_INVALID_ARG
     assert L.bs_lse_merge(ref(d), 0x1000, 0x2000, None, 0x4000, 0x5000, 0x6000, None) == B.BS_ERR_INVALID_ARG
     assert L.bs_lse_merge(ref(d), 0x1004, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == B.BS_ERR_ALIGN
     assert L.bs_lse_merge(ref(_dims(page_size=8)), 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, None) == \

@@ -41,8 +41,8 @@ int main(void) {
   printf("cfg_long %d\n", (int)bs_check_head_cfg(&d, &c, lens));
 
   /* Rejected on the host before anything is enqueued. */
-  printf("attn_null %d\n", (int)bs_sparse_decode_attn(&d, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0,
-                                                      NULL, NULL));
+  printf("attn_null %d\n", (int)bs_sparse_decode_attn(&d, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                                                      NULL, 0, NULL, NULL));
   d.head_dim = 96;
   printf("ws_bad %zu\n", bs_workspace_size(&d));
   printf("setdiff_shape %d\n", (int)bs_block_setdiff(&d, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,

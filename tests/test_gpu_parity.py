@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 import torch
 
-from _parity import run_parity
+from _parity import ATT_ABS, ATT_REL, LSE_ABS, attention_errors, run_parity
 from long_context_serving_gb300 import bsattn as B
 from long_context_serving_gb300.build import build
 from long_context_serving_gb300.layer import PagedLayer
@@ -218,6 +218,112 @@ def test_parity_full_size(cfg, fused):
     rep = run_parity(wl, None, summary_rows_sample=None if cfg <= 2 else 256, fused=fused, attend_units=attend)
     assert rep.selection_checks == wl.U * wl.steps
     rep.check()
+
+
+# ---------------------------------------------------------------------------
+# ED-DMA attention: each block's eviction logit added to its tokens' logits
+# ("Technisches Resümee: NOSA", Methodik / 1. Algorithmus: NOSA, ED-DMA)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,cfg,kw", [("cluster-16-units", 5, dict(B=2, T=2040, steps=6)),
+                                         ("balanced-32-units", 5, dict(B=4, T=2040, steps=16))])
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_ed_dma(name, cfg, kw, fused):
+    rep = run_parity(make_workload(cfg, seed=41, **kw), fused=fused, ed_dma=True)
+    rep.check()
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_ed_dma_full_size(fused):
+    """Config 5 at full size (512 dual units, 16 steps) with ED-DMA attention: every
+    unit's selection at every step, the attention of six sampled units."""
+    wl = _full_workload(5)
+    rep = run_parity(wl, None, summary_rows_sample=256, fused=fused, attend_units=set(_sample_units(wl, 6)),
+                     ed_dma=True)
+    assert rep.selection_checks == wl.U * wl.steps
+    rep.check()
+
+
+def _random_block_logits(layer, rng, sel):
+    """Random logits N(0, 2^2) per block, with one selected block per unit and (with
+    more than one unit) every block of unit 1 at -inf."""
+    U, MB = layer.wl.U, layer.max_blocks
+    e = (rng.standard_normal((U, MB)) * 2).astype(np.float32)
+    for u in range(U):
+        if sel[u]:
+            e[u, sel[u][len(sel[u]) // 2]] = -np.inf
+    if U > 1:
+        e[1, :] = -np.inf
+    return e
+
+
+@pytest.mark.parametrize("name,cfg,kw", [("fp32-cluster", 1, {}), ("fp32-workspace", 1, dict(B=24, T=9000)),
+                                         ("bf16-cluster", 2, dict(T=4133)),
+                                         ("bf16-balanced", 4, dict(B=6, T_range=(3000, 6000))),
+                                         ("bf16-balanced-1200-pages", 2, dict(T=20000))])
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_ed_dma_block_logits_every_plan(name, cfg, kw, noalloc):
+    """bs_sparse_decode_attn with random block logits (some -inf, one unit all -inf)
+    over the oracle's selection, in each attention plan, against ed_dma_attention."""
+    wl = make_workload(cfg, seed=42, **kw)
+    if name == "fp32-workspace":
+        wl.k[:] = 70                     # ~290 pages per unit over 24 units: the workspace plan
+    if name == "bf16-balanced-1200-pages":
+        wl.k[4:] = 600                   # above 1024 pages per unit
+    layer = PagedLayer(wl)
+    layer.prefill()
+    layer.append(0)
+    state = O.init_state(wl)
+    res = O.decode_step(wl, 0, state, attend_units=set())
+    sel = {u: res[u].sel.sel for u in range(wl.U)}
+    layer.set_selection(sel)
+    e = _random_block_logits(layer, np.random.default_rng(6), sel)
+    e_d = torch.as_tensor(e, device=layer.device)
+    kv = layer.kv_at(layer.seq_lens[0])
+    if noalloc:
+        B.sparse_decode_attn_noalloc(layer.dims, layer.q[0], kv, layer.cfg, layer.sel[layer.cur],
+                                     layer.cnt[layer.cur], layer.out, layer.lse, layer.status, evict_bias=e_d)
+    else:
+        B.sparse_decode_attn(layer.dims, layer.q[0], kv, layer.cfg, layer.sel[layer.cur], layer.cnt[layer.cur],
+                             layer.out, layer.lse, layer.workspace, layer.status, evict_bias=e_d)
+    torch.cuda.synchronize()
+    assert layer.read_status() == 0
+    out, lse = layer.out.cpu().numpy(), layer.lse.cpu().numpy()
+    for u in range(wl.U):
+        b, hk = divmod(u, wl.Hkv)
+        rows = slice(hk * wl.G, (hk + 1) * wl.G)
+        T = int(wl.T(0, b))
+        o_ref, l_ref = O.ed_dma_attention(wl.q64(0, u), wl.K64(u), wl.V64(u), sel[u], int(wl.g[u]), T,
+                                          e[u].astype(np.float64))
+        if np.all(np.isneginf(l_ref)):
+            assert np.all(out[b, rows] == 0) and np.all(np.isneginf(lse[b, rows])), u
+            continue
+        a_abs, a_rel = attention_errors(out[b, rows], o_ref)
+        assert a_abs <= ATT_ABS and a_rel <= ATT_REL, (u, a_abs, a_rel)
+        assert np.abs(lse[b, rows] - l_ref).max() <= LSE_ABS, u
+
+
+def test_ed_dma_zero_logits_equal_plain_bitwise():
+    """All-zero block logits give bitwise the plain attention (adding 0 changes no
+    logit), in the fused step and in the stand-alone call."""
+    wl = make_workload(5, seed=43, B=4, T=2040, steps=3)
+    a, b = PagedLayer(wl), PagedLayer(wl, ed_dma=True)
+    b.evict.zero_()                     # also the selection's logits: both sides select alike
+    a.evict.zero_()
+    a.prefill()
+    b.prefill()
+    for step in range(wl.steps):
+        a.append(step)
+        b.append(step)
+        a.fused_step(step)
+        b.fused_step(step)
+        torch.cuda.synchronize()
+        assert a.selection(1 - a.cur) == b.selection(1 - b.cur), step
+        assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse), step
+    a.attend(wl.steps - 1)
+    b.attend(wl.steps - 1)
+    torch.cuda.synchronize()
+    assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+    assert a.read_status() == 0 and b.read_status() == 0
 
 
 def test_batch_invariance():

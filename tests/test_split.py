@@ -81,6 +81,48 @@ def test_cpu_attention_matches_oracle(cfg_id, kw):
     _compare(wl, 0, out, lse, a, T_of)
 
 
+def test_cpu_attention_ed_dma_matches_oracle():
+    """The host attention with ED-DMA block logits (the eviction logits added to the
+    logits of each block's tokens; one block per unit at -inf, one unit with every
+    listed block at -inf) against the oracle's ed_dma_attention."""
+    build()
+    wl = make_workload(5, seed=33, B=2, T=3000, steps=1)
+    layer = PagedLayer(wl, device="cpu", preload_all=True, ed_dma=True)
+    rng = np.random.default_rng(5)
+    T_of = lambda u: int(wl.T(0, u // wl.Hkv))  # noqa: E731
+    sel, _, _ = _subsets(wl, rng, T_of, layer.max_sel)
+    bias = layer.evict.numpy().copy()
+    e = {u: np.asarray(wl.evict[u], np.float64).copy() for u in range(wl.U)}
+    for u in range(wl.U):
+        c = sel[u][len(sel[u]) // 2]
+        bias[u, c] = -np.inf
+        e[u][c] = -np.inf
+    bias[1, :] = -np.inf
+    e[1][:] = -np.inf
+    idx, cnt = _rows(sel, wl.U, layer.max_sel)
+    out = np.zeros((wl.B, wl.Hq, wl.d), np.float32)
+    lse = np.zeros((wl.B, wl.Hq), np.float32)
+    seq = layer.seq_lens[0].contiguous()
+    host = B.HostKV(k_pool=layer.k_pool.data_ptr(), v_pool=layer.v_pool.data_ptr(), page_table=0,
+                    n_pages=int(wl.n_pages))
+    tables = B.HostTables(page_table=layer.page_table.data_ptr(), seq_lens=seq.data_ptr(),
+                          block_tokens=layer.cfg_arrays["block_tokens"].data_ptr(),
+                          evict_bias=bias.ctypes.data, max_blocks_per_unit=layer.max_blocks)
+    B.cpu_sparse_attn(layer.dims, layer.q[0].contiguous(), host, tables, idx, cnt, out, lse, 4)
+    for u in range(wl.U):
+        b, hk = u // wl.Hkv, u % wl.Hkv
+        rows = slice(hk * wl.G, (hk + 1) * wl.G)
+        o_ref, l_ref = O.ed_dma_attention(wl.q64(0, u), wl.K64(u), wl.V64(u), sel[u], int(wl.g[u]), T_of(u), e[u])
+        o, lv = np.asarray(out[b, rows], np.float64), np.asarray(lse[b, rows], np.float64)
+        if np.all(np.isneginf(l_ref)):
+            assert np.all(o == 0) and np.all(np.isneginf(lv)), u
+            continue
+        diff = np.abs(o - o_ref)
+        assert diff.max() <= ATT_ABS, (u, diff.max())
+        assert (diff / np.maximum(np.abs(o_ref), REL_FLOOR)).max() <= ATT_REL, u
+        assert np.abs(lv - l_ref).max() <= LSE_ABS, u
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("cfg_id,kw", [(2, dict(T=5000)), (5, dict(B=2, T=3000, steps=1)),
                                        (3, dict(B=1, T=9000, steps=1))])

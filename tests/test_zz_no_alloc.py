@@ -86,6 +86,6 @@ def test_noalloc_refuses_dims_beyond_its_scratch():
     assert B.workspace_size(big) > 8 << 20
     status = B.lib().bs_sparse_decode_attn_noalloc(
         B.ctypes.byref(big), layer.q[0].data_ptr(), B.ctypes.byref(layer.kv_at(layer.seq_lens[0])),
-        B.ctypes.byref(layer.cfg), layer.sel[0].data_ptr(), layer.cnt[0].data_ptr(), layer.out.data_ptr(),
+        B.ctypes.byref(layer.cfg), layer.sel[0].data_ptr(), layer.cnt[0].data_ptr(), None, layer.out.data_ptr(),
         layer.lse.data_ptr(), layer.status.data_ptr(), None)
     assert status == B.BS_ERR_CAPACITY
