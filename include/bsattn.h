@@ -295,7 +295,9 @@ typedef struct {
   int32_t *dev_status;
 } bs_step_io;
 
-/* One decode step of one layer: a1, a2, a3, a4 and a5 in two launches.
+/* One decode step of one layer: a1, a2, a3, a4 and a5 in two launches (three in the
+ * attention's balanced mode when a unit can have more than 2048 candidate blocks;
+ * bs_decode_step_launches says which).
  * The results are those of bs_score_blocks, bs_select_topk, bs_sparse_decode_attn and
  * bs_block_setdiff called in that order, plus the a1 update of the one sub-block that
  * holds token T-1 (call bs_build_block_summaries first if more than one token was

@@ -117,9 +117,11 @@ size_t bs_workspace_size(const bs_dims *dims) {
 int bs_decode_step_launches(const bs_dims *dims) {
   if (bsi::check_dims(dims) != BS_OK) return 0;
   const int units = dims->batch * dims->n_kv_heads;
-  // Balanced mode: scores, selection, attention; otherwise the front kernel (scores and
-  // selection) and the attention.
-  return bsi::attn_mode(units, dims->max_gather_pages_per_unit, dims->kv_dtype) == bsi::kModeBalanced ? 3 : 2;
+  // Scores, selection, attention; or the front kernel (scores and selection) and the
+  // attention.
+  return bsi::step_selects_apart(units, dims->max_gather_pages_per_unit, dims->kv_dtype, dims->max_blocks_per_unit)
+             ? 3
+             : 2;
 }
 
 bs_status bs_check_head_cfg(const bs_dims *dims, const bs_head_cfg *c, const int32_t *seq_lens_host) {

@@ -76,6 +76,17 @@ __host__ __device__ inline int attn_mode(int units, int max_gather_pages, int kv
   return attn_cluster_mode(units, max_gather_pages) ? kModeCluster : kModeWorkspace;
 }
 
+// The fused decode step selects in a kernel of its own (three launches: scores,
+// selection, attention) in balanced mode when a unit can have more candidates than
+// kFrontSelectMaxCandidates (eight per thread of a front CTA); otherwise the front
+// kernel's CTA that finishes a unit's last score tile selects it (two launches).
+constexpr int kFrontSelectMaxCandidates = 2048;
+__host__ __device__ inline bool step_selects_apart(int units, int max_gather_pages, int kv_dtype, int max_blocks) {
+  // (the tail block is always forced: at most max_blocks - 1 candidates)
+  return attn_mode(units, max_gather_pages, kv_dtype) == kModeBalanced &&
+         max_blocks - 1 > kFrontSelectMaxCandidates;
+}
+
 // Floats of the workspace before the split records (the counters, and the page lists
 // in balanced mode), and the floats of the records themselves.
 __host__ __device__ inline size_t attn_records_offset(size_t units, int max_gather_pages, int mode) {

@@ -38,8 +38,10 @@ struct __align__(16) SelShared {  // hist is cleared with 16-byte stores
   uint32_t hist[kBuckets];      // the radix passes use the first 256
   int warp_tot[kWarps];
   int wt[2][kWarps];            // warp totals of the one-barrier scan, two buffers
+  int wt2[2][kWarps];           // their inclusive prefix (CTAs of more than 8 warps)
   uint32_t warp_min[kWarps], warp_max[kWarps];
   int warp_cnt[kWarps];
+  uint32_t mm[4];               // CTA-wide min, max, count (CTAs of more than 8 warps)
   int bcast[4];
   int bnd_n;
   int bnd_idx[kBndDirect];
@@ -400,8 +402,10 @@ __device__ __noinline__ int compact_selection(const uint8_t *flags, int n_blk, i
 // ranking of the taken candidates by ballots per (round, warp) and one prefix scan.
 // ---------------------------------------------------------------------------
 
-// Exclusive prefix sum over the CTA with one barrier. Two consecutive calls with the
-// same `buf` need a barrier between them. *total gets the sum.
+// Exclusive prefix sum over the CTA. Up to 8 warps: one barrier, after which every
+// thread adds the warp totals itself; two consecutive calls with the same `buf` need a
+// barrier between them. More warps: warp 0 scans the warp totals between two barriers
+// (every thread then reads two values instead of one per warp). *total gets the sum.
 template <int NT>
 __device__ __forceinline__ int block_scan1(int v, SelShared<NT> &sh, int buf, int *total) {
   constexpr int W = NT / 32;
@@ -415,17 +419,33 @@ __device__ __forceinline__ int block_scan1(int v, SelShared<NT> &sh, int buf, in
   if (lane == 31) sh.wt[buf][warp] = x;
   __syncthreads();
   int off = 0, tot = 0;
+  if constexpr (W <= 8) {
 #pragma unroll
-  for (int w = 0; w < W; ++w) {
-    const int t = sh.wt[buf][w];
-    off += w < warp ? t : 0;
-    tot += t;
+    for (int w = 0; w < W; ++w) {
+      const int t = sh.wt[buf][w];
+      off += w < warp ? t : 0;
+      tot += t;
+    }
+  } else {
+    if (warp == 0) {
+      int w = lane < W ? sh.wt[buf][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < W) sh.wt2[buf][lane] = w;   // inclusive
+    }
+    __syncthreads();
+    off = warp > 0 ? sh.wt2[buf][warp - 1] : 0;
+    tot = sh.wt2[buf][W - 1];
   }
   *total = tot;
   return off + x - v;
 }
 
-// CTA-wide min, max and sum with one barrier (results in every thread).
+// CTA-wide min, max and sum (results in every thread): one barrier up to 8 warps, two
+// beyond (warp 0 reduces the warp values).
 template <int NT>
 __device__ __forceinline__ void block_min_max_count(uint32_t &kmin, uint32_t &kmax, int &cnt, SelShared<NT> &sh) {
   constexpr int W = NT / 32;
@@ -439,14 +459,31 @@ __device__ __forceinline__ void block_min_max_count(uint32_t &kmin, uint32_t &km
     sh.warp_cnt[warp] = cnt;
   }
   __syncthreads();
-  kmin = 0xffffffffu;
-  kmax = 0u;
-  cnt = 0;
+  if constexpr (W <= 8) {
+    kmin = 0xffffffffu;
+    kmax = 0u;
+    cnt = 0;
 #pragma unroll
-  for (int w = 0; w < W; ++w) {
-    kmin = min(kmin, sh.warp_min[w]);
-    kmax = max(kmax, sh.warp_max[w]);
-    cnt += sh.warp_cnt[w];
+    for (int w = 0; w < W; ++w) {
+      kmin = min(kmin, sh.warp_min[w]);
+      kmax = max(kmax, sh.warp_max[w]);
+      cnt += sh.warp_cnt[w];
+    }
+  } else {
+    if (warp == 0) {
+      const uint32_t a = __reduce_min_sync(0xffffffffu, lane < W ? sh.warp_min[lane] : 0xffffffffu);
+      const uint32_t b = __reduce_max_sync(0xffffffffu, lane < W ? sh.warp_max[lane] : 0u);
+      const uint32_t n = __reduce_add_sync(0xffffffffu, lane < W ? static_cast<uint32_t>(sh.warp_cnt[lane]) : 0u);
+      if (lane == 0) {
+        sh.mm[0] = a;
+        sh.mm[1] = b;
+        sh.mm[2] = n;
+      }
+    }
+    __syncthreads();
+    kmin = sh.mm[0];
+    kmax = sh.mm[1];
+    cnt = static_cast<int>(sh.mm[2]);
   }
 }
 

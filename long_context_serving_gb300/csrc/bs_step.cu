@@ -182,18 +182,30 @@ __device__ __forceinline__ void unit_select_publish(const bs_dims &dims, const b
     const int tail_pages = min(ppb, (T - (ge.n_blk - 1) * g + kPage - 1) / kPage);
     const int n_pages = total > 0 ? (total - 1) * ppb + tail_pages : 0;
     int32_t *pl = plist + static_cast<size_t>(u) * dims.max_gather_pages_per_unit;
-    if (n_pages <= dims.max_gather_pages_per_unit)
-      for (int i = tid; i < n_pages; i += NT) {
-        const int blk = i / ppb, pb = i - blk * ppb;
-        const int c = cur_sm[blk];
-        const int lp = c * ppb + pb;
-        int phys = -1;
-        if (c >= 0 && lp < n_lp && c * g + pb * kPage < T) {
-          phys = lp < pt_in_smem ? pt_sm[pt_lead + lp] : __ldg(pt_row + lp);
-          if (phys < 0 || phys >= dims.n_pages) phys = -1;
+    if (n_pages <= dims.max_gather_pages_per_unit) {
+      // Four entries a thread per round, their page-table loads issued before any store.
+      constexpr int kB = 4;
+      for (int i0 = tid; i0 < n_pages; i0 += NT * kB) {
+        int phys[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = i0 + j * NT;
+          phys[j] = -1;
+          if (i < n_pages) {
+            const int blk = i / ppb, pb = i - blk * ppb;
+            const int c = cur_sm[blk];
+            const int lp = c * ppb + pb;
+            if (c >= 0 && lp < n_lp && c * g + pb * kPage < T)
+              phys[j] = lp < pt_in_smem ? pt_sm[pt_lead + lp] : __ldg(pt_row + lp);
+          }
         }
-        pl[i] = phys;
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          const int i = i0 + j * NT;
+          if (i < n_pages) pl[i] = (phys[j] < 0 || phys[j] >= dims.n_pages) ? -1 : phys[j];
+        }
       }
+    }
   }
   // Publish: the row and the page list are written; the count (release) tells the
   // attention they are ready.
@@ -374,8 +386,10 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
 
 // ---------------------------------------------------------------------------
 // Fused step in balanced mode (the attention's balanced plan: more than 19 units or
-// selections above 1024 pages, up to 1024 units): three launches, each a programmatic
-// dependent of the one before.
+// selections above 1024 pages, up to 1024 units) when a unit can have more than
+// kFrontSelectMaxCandidates candidates: three launches, each a programmatic dependent
+// of the one before. (With fewer, the front kernel below selects, as in the other
+// modes: two launches.)
 //   1. step_score_balanced: a persistent grid; the score tiles (64 summary rows) of
 //      every retrieval and dual unit, in unit order, form one stream cut into equal
 //      contiguous shares, one per CTA; a CTA streams its tiles through a ring of nbuf
@@ -608,7 +622,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
   }
   const StepWords words = step_words(io.workspace, units);
   int32_t *plist = lists ? words.tickets + attn_counter_floats(units) : nullptr;
-  if (mode == kModeBalanced) {
+  if (step_selects_apart(units, dims.max_gather_pages_per_unit, dims.kv_dtype, dims.max_blocks_per_unit)) {
     // 1. balanced scores: the ring of nbuf score tiles, the queries and dot products,
     //    then the plan; nbuf 2 or 3, whichever gives more tiles in flight per SM
     //    (preferring more CTAs).
