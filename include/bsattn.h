@@ -203,11 +203,11 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * Split-KV: a unit's gathered pages are cut into contiguous pieces; each piece keeps an
  * fp32 online softmax and the partials are merged by log-sum-exp in a fixed order, so
  * the result does not depend on timing. Three plans, chosen from the dims:
- *   - cluster mode (at most 19 units with max_gather_pages_per_unit <= 1024; for fp32
- *     caches also at least 304 units, or max_gather_pages_per_unit <= 256): every unit
- *     gets S splits, S the largest power of two <= 16 with units * S <= two CTAs per SM;
- *     the S CTAs of a unit form one thread-block cluster and merge through distributed
- *     shared memory; split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
+ *   - cluster mode (max_gather_pages_per_unit <= 1024 with at most 19 units, at least
+ *     304 units, or max_gather_pages_per_unit <= 256): every unit gets S splits, S the
+ *     largest power of two <= 16 with units * S <= two CTAs per SM; the S CTAs of a
+ *     unit form one thread-block cluster and merge through distributed shared memory;
+ *     split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
  *   - balanced mode (bf16 caches otherwise, up to 1024 units): the selected pages of
  *     all units, in unit order, form one stream of W pages, cut into P' = min(P, W)
  *     equal contiguous shares, one per CTA of a persistent grid of P CTAs (as many as
@@ -250,8 +250,8 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * until the process exits.
  * Limit: bs_workspace_size(dims) must not exceed 8 MiB; larger dims return
  * BS_ERR_CAPACITY before anything is enqueued. At head_dim 128 with bf16 caches in
- * balanced mode that allows, with 1024 pages per unit, all 1,024 units of the plan at
- * G = 4 (746 at G = 8); with 2048 pages per unit, 708 units at G = 4 (500 at G = 8).
+ * balanced mode that allows, with 512 pages per unit, every launch of the plan (20 to
+ * 303 units, G <= 8); with 2048 pages per unit, 708 units at G = 4 (500 at G = 8).
  * The first call on each device looks up the array's device address with that device
  * current and caches it; make that first call before any stream capture. The cached
  * address belongs to the device's context at that time: after cudaDeviceReset (or

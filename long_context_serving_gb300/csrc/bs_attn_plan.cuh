@@ -45,12 +45,15 @@ constexpr int kClusterUnitsMax = 19; // cluster mode while units x 16 splits fit
 constexpr int kManyUnits = 304;      // ... or once the units alone fill it (then one split each)
 
 // Attention modes.
-//   cluster:   few units with small selections (bf16 and fp32 caches); a unit's S splits
+//   cluster:   selections up to 1024 pages with few units (<= 19), many units (>= 304)
+//              or selections up to 256 pages (bf16 and fp32 caches); a unit's S splits
 //              are one thread-block cluster and merge through distributed shared memory;
-//   balanced:  every other bf16 launch up to kWsMaxUnits units: the pages of all units
-//              form one stream cut into equal contiguous shares, one per CTA of a
-//              persistent grid; a unit's pieces merge through split records in the
-//              workspace (the last piece to finish merges);
+//   balanced:  every other bf16 launch up to kWsMaxUnits units (20..303 units with
+//              larger selections, or selections above 1024 pages, whose page counts can
+//              differ a lot between units): the pages of all units form one stream cut
+//              into equal contiguous shares, one per CTA of a persistent grid; a unit's
+//              pieces merge through split records in the workspace (the last piece to
+//              finish merges);
 //   workspace: the rest (fp32 caches beyond cluster mode, bf16 beyond kWsMaxUnits).
 enum AttnMode { kModeCluster = 0, kModeBalanced = 1, kModeWorkspace = 2 };
 constexpr int kWsMaxUnits = 1024;  // units the balanced plan takes (page offsets in shared memory)
@@ -70,7 +73,7 @@ __host__ __device__ inline bool attn_cluster_mode(int units, int max_gather_page
 
 __host__ __device__ inline int attn_mode(int units, int max_gather_pages, int kv_dtype) {
   if (kv_dtype == BS_BF16) {
-    if (units <= kClusterUnitsMax && max_gather_pages <= kClusterMaxPages) return kModeCluster;
+    if (attn_cluster_mode(units, max_gather_pages)) return kModeCluster;
     if (units <= kWsMaxUnits) return kModeBalanced;
   }
   return attn_cluster_mode(units, max_gather_pages) ? kModeCluster : kModeWorkspace;

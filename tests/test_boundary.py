@@ -89,20 +89,23 @@ def test_workspace_size_modes():
     def workspace(u, G):
         return counters(u) + u * 32 * G * (128 + 4) * 4
 
-    assert _ws(8, 4, 1024) == counters(8) + plist(8, 1024)          # few units, small selections: cluster
+    assert _ws(8, 4, 1024) == counters(8) + plist(8, 1024)          # few units: cluster
     assert _ws(19, 4, 1024) == counters(19) + plist(19, 1024)
+    assert _ws(20, 4, 256) == counters(20) + plist(20, 256)         # small selections: cluster
+    assert _ws(304, 4, 1024) == counters(304) + plist(304, 1024)    # many units: cluster
     assert _ws(8, 4, 1025) == balanced(8, 4, 1025)                  # above 1024 pages
-    assert _ws(20, 4, 16) == balanced(20, 4, 16)                    # more than 19 units
-    assert _ws(1024, 7, 512) == balanced(1024, 7, 512)
-    assert _ws(1025, 4, 512) == counters(1025) + plist(1025, 512)   # beyond the balanced plan: one CTA per unit
+    assert _ws(20, 4, 257) == balanced(20, 4, 257)                  # 20..303 units, larger selections
+    assert _ws(303, 4, 512) == balanced(303, 4, 512)
+    assert _ws(1024, 7, 1025) == balanced(1024, 7, 1025)
+    assert _ws(1025, 4, 512) == counters(1025) + plist(1025, 512)   # many units: cluster
     assert _ws(1025, 4, 2048) == workspace(1025, 4)
     # fp32 caches keep the cluster / workspace plan
     assert _ws(8, 4, 2048, B.BS_FP32) == workspace(8, 4)
     assert _ws(100, 4, 512, B.BS_FP32) == workspace(100, 4)
     assert _ws(100, 4, 256, B.BS_FP32) == counters(100) + plist(100, 256)
     limit = 8 << 20
-    assert _ws(1024, 4, 1024) <= limit
-    assert _ws(746, 8, 1024) <= limit < _ws(747, 8, 1024)
+    assert _ws(303, 8, 512) <= limit                                # every balanced launch at 512 pages
+    assert _ws(1024, 4, 1024) <= limit                              # (cluster)
     assert _ws(708, 4, 2048) <= limit < _ws(709, 4, 2048)
     assert _ws(500, 8, 2048) <= limit < _ws(501, 8, 2048)
 

@@ -225,10 +225,15 @@ def test_parity_full_size(cfg, fused):
 # ("Technisches Resümee: NOSA", Methodik / 1. Algorithmus: NOSA, ED-DMA)
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("name,cfg,kw", [("cluster-16-units", 5, dict(B=2, T=2040, steps=6)),
-                                         ("balanced-32-units", 5, dict(B=4, T=2040, steps=16))])
+                                         ("cluster-32-units", 5, dict(B=4, T=2040, steps=16)),
+                                         ("balanced-32-units", 5, dict(B=4, T=8190, steps=4))])
 @pytest.mark.parametrize("fused", [False, True])
 def test_parity_ed_dma(name, cfg, kw, fused):
-    rep = run_parity(make_workload(cfg, seed=41, **kw), fused=fused, ed_dma=True)
+    wl = make_workload(cfg, seed=41, **kw)
+    if name.startswith("balanced"):
+        wl.k[:] = 80                    # selections above 256 pages over 32 units: the balanced plan
+        wl.k_e[:] = 60
+    rep = run_parity(wl, fused=fused, ed_dma=True)
     rep.check()
 
 
@@ -267,6 +272,8 @@ def test_ed_dma_block_logits_every_plan(name, cfg, kw, noalloc):
     wl = make_workload(cfg, seed=42, **kw)
     if name == "fp32-workspace":
         wl.k[:] = 70                     # ~290 pages per unit over 24 units: the workspace plan
+    if name == "bf16-balanced":
+        wl.k[:] = 80                     # ~330 pages per unit over 24 units: the balanced plan
     if name == "bf16-balanced-1200-pages":
         wl.k[4:] = 600                   # above 1024 pages per unit
     layer = PagedLayer(wl)

@@ -9,11 +9,11 @@ reads BS_ERR_TIMEOUT. Nothing faults: the failure is made on the host, in a buff
 caller owns. After zeroing the workspace, the same layer runs the step again and
 matches the float64 oracle.
 
-The layer here (8 units) takes the plan with a thread-block cluster per unit, whose
-front kernel elects a selecting CTA per unit through those tickets. With more units the
-step selects every unit in a kernel of its own (one CTA per unit, no tickets), so no
-buffer the caller owns can hold a selection back; its attention waits through the same
-bounded wait function.
+The layer here (8 units) takes the plan whose front kernel elects a selecting CTA per
+unit through those tickets. The plan for more than 2048 candidates a unit selects every
+unit in a kernel of its own (one CTA per unit, no tickets), so no buffer the caller owns
+can hold a selection back there; its attention waits through the same bounded wait
+function.
 """
 import numpy as np
 import pytest
