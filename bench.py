@@ -634,7 +634,7 @@ def run_ours(args) -> None:
     # each a programmatic dependent of the one before (overlapping), timed as one.
     roofline = {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(layer_gbs / peak, 4), "traffic": None,
-                "kernel": (f"bs_decode_step = {step_kernels(wl, bn.launches_per_layer, bn.layers[0].dims)} (one layer step; "
+                "kernel": (f"bs_decode_step = {step_kernels(wl, bn.launches_per_layer)} (one layer step; "
                            "the launches overlap through programmatic dependent launch)" if args.path == "fused"
                            else "the five calls of one layer step"),
                 "peak_source": peak_note, "algorithmic_bytes_per_launch": nbytes["layer_step"],
@@ -735,14 +735,10 @@ def bn_launches(path: str, layer, B) -> int:
     return n
 
 
-def step_kernels(wl, launches: int, dims) -> str:
-    """The kernels of one bs_decode_step call, in launch order (the attention's balanced
-    plan: bf16 caches with more than 19 units or selections above 1024 pages)."""
-    if wl.dtype != "bf16":
-        return "step_front_kernel + attn_ffma_kernel"
-    balanced = wl.U > 19 or dims.max_gather_pages_per_unit > 1024
+def step_kernels(wl, launches: int) -> str:
+    """The kernels of one bs_decode_step call, in launch order."""
     front = "step_score_balanced + step_select_kernel" if launches == 3 else "step_front_kernel"
-    return f"{front} + {'attn_ws_kernel' if balanced else 'attn_mma_kernel'}"
+    return f"{front} + {'attn_mma_kernel' if wl.dtype == 'bf16' else 'attn_ffma_kernel'}"
 
 
 def main():

@@ -202,26 +202,18 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * the entries of selected blocks are read.
  * Split-KV: a unit's gathered pages are cut into contiguous pieces; each piece keeps an
  * fp32 online softmax and the partials are merged by log-sum-exp in a fixed order, so
- * the result does not depend on timing. Three plans, chosen from the dims:
+ * the result does not depend on timing. Two plans, chosen from the dims:
  *   - cluster mode (max_gather_pages_per_unit <= 1024 with at most 19 units, at least
  *     304 units, or max_gather_pages_per_unit <= 256): every unit gets S splits, S the
  *     largest power of two <= 16 with units * S <= two CTAs per SM; the S CTAs of a
  *     unit form one thread-block cluster and merge through distributed shared memory;
  *     split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
- *   - balanced mode (bf16 caches otherwise, up to 1024 units): the selected pages of
- *     all units, in unit order, form one stream of W pages, cut into P' = min(P, W)
- *     equal contiguous shares, one per CTA of a persistent grid of P CTAs (as many as
- *     fit on the GPU at once, at most 512); the pieces of a unit merge through split
- *     records in the workspace, the last piece to finish merging them in CTA order;
  *   - workspace mode (the rest): each unit's splits are sized by its own page count,
  *     p = max(4 * ceil(pages / 128), m) pages per split (m = 32, or 4 when
  *     max_gather_pages_per_unit > 1024), so at most 32 splits; partials go through the
  *     workspace and the last split to finish merges them.
- * In cluster and workspace mode a unit's plan depends on its own sizes only, so a
- * sub-batch launched with the same S gives bitwise the same per-unit results as the full
- * batch; in balanced mode the shares depend on every unit's page count, so a sub-batch
- * can differ from the full batch in the last bits of the attention output (never in a
- * selection), while repeated runs on the same inputs are bitwise equal.
+ * A unit's plan depends on its own sizes only, so a sub-batch launched with the same S
+ * gives bitwise the same per-unit results as the full batch.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
  * aligned. It starts with four int32 words per unit (padded to 16 bytes): the fused
  * step's selection tickets, the attention's arrival tickets, the fused step's published
@@ -229,9 +221,8 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  * call: zero the workspace once after allocating it. Every call that completes leaves
  * the tickets zero again; after a call that reported BS_ERR_TIMEOUT, zero the workspace
  * again. Then, by mode: cluster mode the fused step's page lists (int32 [units]
- * [max_gather_pages_per_unit]); balanced mode the page lists, then one split record of
- * G * (head_dim + 4) floats per (unit + CTA) for units + 512 records; workspace mode 32
- * split records per unit. The rest is overwritten per call.
+ * [max_gather_pages_per_unit]); workspace mode 32 split records of G * (head_dim + 4)
+ * floats per unit. The rest is overwritten per call.
  * Calls that share a workspace must not run concurrently. */
 bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv *kv,
                                 const bs_head_cfg *cfg, const int32_t *sel_idx,
@@ -249,9 +240,10 @@ bs_status bs_sparse_decode_attn(const bs_dims *dims, const void *q, const bs_kv 
  * inside this library's device memory, which every GPU that loads the library keeps
  * until the process exits.
  * Limit: bs_workspace_size(dims) must not exceed 8 MiB; larger dims return
- * BS_ERR_CAPACITY before anything is enqueued. At head_dim 128 with bf16 caches in
- * balanced mode that allows, with 512 pages per unit, every launch of the plan (20 to
- * 303 units, G <= 8); with 2048 pages per unit, 708 units at G = 4 (500 at G = 8).
+ * BS_ERR_CAPACITY before anything is enqueued. In workspace mode the split records
+ * take 67.6 KB per unit at head_dim 128, G = 4: at most 124 units (62 at G = 8); in
+ * cluster mode (counters and page lists, 16 + 4 * max_gather_pages_per_unit bytes per
+ * unit) 2,040 units at 1024 pages per unit.
  * The first call on each device looks up the array's device address with that device
  * current and caches it; make that first call before any stream capture. The cached
  * address belongs to the device's context at that time: after cudaDeviceReset (or
@@ -296,7 +288,7 @@ typedef struct {
 } bs_step_io;
 
 /* One decode step of one layer: a1, a2, a3, a4 and a5 in two launches (three in the
- * attention's balanced mode when a unit can have more than 2048 candidate blocks;
+ * attention's workspace mode when a unit can have more than 2048 candidate blocks;
  * bs_decode_step_launches says which).
  * The results are those of bs_score_blocks, bs_select_topk, bs_sparse_decode_attn and
  * bs_block_setdiff called in that order, plus the a1 update of the one sub-block that

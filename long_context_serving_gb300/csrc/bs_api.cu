@@ -106,12 +106,11 @@ size_t bs_workspace_size(const bs_dims *dims) {
   const size_t units = static_cast<size_t>(dims->batch) * dims->n_kv_heads;
   const int mg = dims->max_gather_pages_per_unit;
   // Cluster mode keeps the split partials on chip: the counters and the fused step's
-  // page lists. Balanced mode: the counters, the page lists and one split record per
-  // (unit + CTA). Workspace mode: the counters and 32 split records per unit.
-  const int mode = bsi::attn_mode(static_cast<int>(units), mg, dims->kv_dtype);
-  const size_t head = mode == bsi::kModeCluster ? bsi::attn_counter_floats(units) + bsi::attn_plist_ints(units, mg)
-                                                : bsi::attn_records_offset(units, mg, mode);
-  return (head + bsi::attn_record_area_floats(units, G, dims->head_dim, mode)) * sizeof(float);
+  // page lists. Workspace mode: the counters and the split records.
+  const int mode = bsi::attn_mode(static_cast<int>(units), mg);
+  const size_t tail = mode == bsi::kModeCluster ? bsi::attn_plist_ints(units, mg)
+                                                : bsi::attn_record_area_floats(units, G, dims->head_dim, mode);
+  return (bsi::attn_counter_floats(units) + tail) * sizeof(float);
 }
 
 int bs_decode_step_launches(const bs_dims *dims) {
@@ -119,7 +118,7 @@ int bs_decode_step_launches(const bs_dims *dims) {
   const int units = dims->batch * dims->n_kv_heads;
   // Scores, selection, attention; or the front kernel (scores and selection) and the
   // attention.
-  return bsi::step_selects_apart(units, dims->max_gather_pages_per_unit, dims->kv_dtype, dims->max_blocks_per_unit)
+  return bsi::step_selects_apart(units, dims->max_gather_pages_per_unit, dims->max_blocks_per_unit)
              ? 3
              : 2;
 }

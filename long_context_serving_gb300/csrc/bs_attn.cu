@@ -22,8 +22,7 @@ bs_status launch_standalone(const bs_dims *dims, const void *q, const bs_kv *kv,
   a.lse = lse;
   const StepWords w = step_words(ws, units);
   a.arrivals = w.arrivals;
-  a.records = ws + attn_records_offset(units, dims->max_gather_pages_per_unit,
-                                       attn_mode(units, dims->max_gather_pages_per_unit, dims->kv_dtype));
+  a.records = ws + attn_records_offset(units);
   a.plist = nullptr;
   a.pub = nullptr;
   a.expect = nullptr;

@@ -1,12 +1,7 @@
-// Attention kernels for bf16 caches and their launcher: the cluster kernel (tiled TMA
-// + warp-level tensor-core MMA, device code attn_split_mma in bs_attn_impl.cuh; few
-// units with small selections, and the workspace mode beyond the balanced plan's unit
-// limit) and the balanced kernel (device code attn_balanced_mma in bs_attn_ws.cuh;
-// every other launch).
-#include <algorithm>
-
+// Attention kernels for bf16 caches (tiled TMA + warp-level tensor-core MMA, device
+// code attn_split_mma in bs_attn_impl.cuh) and their launcher.
+#include "bs_attn_impl.cuh"
 #include "bs_attn_launch.cuh"
-#include "bs_attn_ws.cuh"
 
 namespace bsi {
 namespace {
@@ -23,54 +18,15 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnArgs a, const
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kWsThreads, 2) attn_ws_kernel(AttnArgs a, const __grid_constant__ CUtensorMap tmk,
-                                                                const __grid_constant__ CUtensorMap tmv, bool step) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  if (step) pdl_launch_dependents();
-  attn_balanced_mma<D, G>(a, &tmk, &tmv, align_smem_1024(smem_raw), step);
-  if (step) pdl_wait();
-}
-
-// CTAs of a balanced launch: as many as fit on the GPU at once (at most kWsMaxCtas).
-template <int D, int G>
-int ws_grid_ctas(int smem) {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_ws_kernel<D, G>, kWsThreads, smem) !=
-            cudaSuccess ||
-        per_sm <= 0)
-      return 0;
-    cached[dev] = std::min(kWsMaxCtas, sms * per_sm);
-  }
-  return cached[dev];
-}
-
-template <int D, int G>
 bs_status launch_modes(const AttnArgs &a, bool step, const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t cs) {
   const int units = a.dims.batch * a.dims.n_kv_heads;
-  const int mode = attn_mode(units, a.dims.max_gather_pages_per_unit, BS_BF16);
-  if (mode == kModeBalanced) {
-    constexpr int kSmem = WsLayout<D>::kBytes + kSmemAlignSlack;
-    auto kernel = attn_ws_kernel<D, G>;
-    static const bool attrs_ok =
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) == cudaSuccess;
-    if (!attrs_ok) return BS_ERR_CUDA;
-    const int ctas = ws_grid_ctas<D, G>(kSmem);
-    if (ctas <= 0) return BS_ERR_CUDA;
-    const cudaError_t e = launch_ex(kernel, dim3(ctas), kWsThreads, kSmem, cs, 0, step, a, tk, tv, step);
-    return e == cudaSuccess ? BS_OK : BS_ERR_CUDA;
-  }
   constexpr int kSmem = MmaLayout<D>::kBytes + kSmemAlignSlack;
   auto kernel = attn_mma_kernel<D, G>;
   static const bool attrs_ok =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) == cudaSuccess &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (!attrs_ok) return BS_ERR_CUDA;
-  const bool cluster = mode == kModeCluster;
+  const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit) == kModeCluster;
   const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
   const dim3 grid(splits, units);
   const cudaError_t e =

@@ -23,7 +23,7 @@ bs_status launch_modes(const AttnArgs &a, bool step, cudaStream_t cs) {
       cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (!attrs_ok) return BS_ERR_CUDA;
   const int units = a.dims.batch * a.dims.n_kv_heads;
-  const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit, BS_FP32) == kModeCluster;
+  const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit) == kModeCluster;
   const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
   const dim3 grid(splits, units);
   const cudaError_t e =

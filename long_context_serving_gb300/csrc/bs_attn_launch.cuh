@@ -16,8 +16,8 @@ struct AttnArgs {
   const float *bias;  // logit bias of every block [units][max_blocks_per_unit] (ED-DMA), or null
   float *out;
   float *lse;
-  int32_t *arrivals;  // per-unit arrival tickets of the splits (workspace and balanced modes)
-  float *records;     // split records (workspace and balanced modes)
+  int32_t *arrivals;  // per-unit arrival tickets of the splits (workspace mode)
+  float *records;     // split records (workspace mode)
   const int32_t *plist;  // fused step: page lists of non-streaming units, else null
   const int32_t *pub;    // fused step: published selections, (epoch << 16) | count, per unit
   int32_t *expect;       // fused step: epoch of the last selection the attention took, per unit

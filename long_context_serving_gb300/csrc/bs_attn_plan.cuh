@@ -23,8 +23,7 @@ __host__ __device__ constexpr int attn_record_floats(int D) { return D + 4; }
 //             attention of the fused step).
 // After them: in cluster mode the fused step's page lists (int32 [units][max gather
 // pages]: the physical pages of each unit's selected blocks in attention order); in
-// balanced mode the page lists, then the split records; in workspace mode the split
-// records.
+// workspace mode the split records.
 __host__ __device__ constexpr size_t attn_counter_floats(size_t units) { return (4 * units + 3) / 4 * 4; }
 __host__ __device__ constexpr size_t attn_plist_ints(size_t units, int max_gather) {
   return (units * static_cast<size_t>(max_gather) + 3) / 4 * 4;
@@ -44,62 +43,42 @@ constexpr int kMidSplitPages = 32;   // workspace mode below 1024 pages: pages p
 constexpr int kClusterUnitsMax = 19; // cluster mode while units x 16 splits fit one wave of ~304 CTAs ...
 constexpr int kManyUnits = 304;      // ... or once the units alone fill it (then one split each)
 
-// Attention modes.
+// Attention modes, chosen from the dims only.
 //   cluster:   selections up to 1024 pages with few units (<= 19), many units (>= 304)
-//              or selections up to 256 pages (bf16 and fp32 caches); a unit's S splits
-//              are one thread-block cluster and merge through distributed shared memory;
-//   balanced:  every other bf16 launch up to kWsMaxUnits units (20..303 units with
-//              larger selections, or selections above 1024 pages, whose page counts can
-//              differ a lot between units): the pages of all units form one stream cut
-//              into equal contiguous shares, one per CTA of a persistent grid; a unit's
-//              pieces merge through split records in the workspace (the last piece to
-//              finish merges);
-//   workspace: the rest (fp32 caches beyond cluster mode, bf16 beyond kWsMaxUnits).
-enum AttnMode { kModeCluster = 0, kModeBalanced = 1, kModeWorkspace = 2 };
-constexpr int kWsMaxUnits = 1024;  // units the balanced plan takes (page offsets in shared memory)
-constexpr int kWsMaxCtas = 512;    // CTAs of a balanced launch the record area is sized for
+//              or selections up to 256 pages; a unit's S splits are one thread-block
+//              cluster and merge through distributed shared memory; every unit has the
+//              same number of splits;
+//   workspace: the rest (selections above 1024 pages, or 20..303 units with selections
+//              that may exceed 8 x 32 pages, whose page counts can then differ a lot
+//              between units): each unit's splits are sized by its own pages (at least
+//              32 per split, so a long unit gets more splits), up to 32, and merge
+//              through records in the workspace.
+enum AttnMode { kModeCluster = 0, kModeWorkspace = 1 };
 
-// Cluster mode: a unit's splits are the CTAs of one cluster and merge through
-// distributed shared memory; every unit has the same number of splits. Workspace mode:
-// selections above 1024 pages, or a middling number of units (20..303) with selections
-// that may exceed 8 x 32 pages, whose page counts can then differ a lot between units:
-// each unit's splits are sized by its own pages (at least 32 per split, so a long unit
-// gets more splits), up to 32, and merge through records in the workspace. The choice
-// depends on the dims only.
 __host__ __device__ inline bool attn_cluster_mode(int units, int max_gather_pages) {
   if (max_gather_pages > kClusterMaxPages) return false;
   return units <= kClusterUnitsMax || units >= kManyUnits || max_gather_pages <= 8 * kMidSplitPages;
 }
 
-__host__ __device__ inline int attn_mode(int units, int max_gather_pages, int kv_dtype) {
-  if (kv_dtype == BS_BF16) {
-    if (attn_cluster_mode(units, max_gather_pages)) return kModeCluster;
-    if (units <= kWsMaxUnits) return kModeBalanced;
-  }
+__host__ __device__ inline int attn_mode(int units, int max_gather_pages) {
   return attn_cluster_mode(units, max_gather_pages) ? kModeCluster : kModeWorkspace;
 }
 
 // The fused decode step selects in a kernel of its own (three launches: scores,
-// selection, attention) in balanced mode when a unit can have more candidates than
+// selection, attention) in workspace mode when a unit can have more candidates than
 // kFrontSelectMaxCandidates (eight per thread of a front CTA); otherwise the front
 // kernel's CTA that finishes a unit's last score tile selects it (two launches).
 constexpr int kFrontSelectMaxCandidates = 2048;
-__host__ __device__ inline bool step_selects_apart(int units, int max_gather_pages, int kv_dtype, int max_blocks) {
+__host__ __device__ inline bool step_selects_apart(int units, int max_gather_pages, int max_blocks) {
   // (the tail block is always forced: at most max_blocks - 1 candidates)
-  return attn_mode(units, max_gather_pages, kv_dtype) == kModeBalanced &&
-         max_blocks - 1 > kFrontSelectMaxCandidates;
+  return attn_mode(units, max_gather_pages) == kModeWorkspace && max_blocks - 1 > kFrontSelectMaxCandidates;
 }
 
-// Floats of the workspace before the split records (the counters, and the page lists
-// in balanced mode), and the floats of the records themselves.
-__host__ __device__ inline size_t attn_records_offset(size_t units, int max_gather_pages, int mode) {
-  return attn_counter_floats(units) + (mode == kModeBalanced ? attn_plist_ints(units, max_gather_pages) : 0);
-}
+// Floats of the workspace before the split records (the counters), and the floats of
+// the records themselves (workspace mode: 32 per unit, index unit, split).
+__host__ __device__ inline size_t attn_records_offset(size_t units) { return attn_counter_floats(units); }
 __host__ __device__ inline size_t attn_record_area_floats(size_t units, int G, int D, int mode) {
-  const size_t rec = static_cast<size_t>(G) * (D + 4);
-  if (mode == kModeBalanced) return (units + kWsMaxCtas) * rec;   // index: unit + CTA
-  if (mode == kModeWorkspace) return units * 32 * rec;            // index: unit, split
-  return 0;
+  return mode == kModeWorkspace ? units * 32 * static_cast<size_t>(G) * (D + 4) : 0;
 }
 
 // Smallest split (pages) in workspace mode.

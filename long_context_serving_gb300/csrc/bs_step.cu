@@ -52,7 +52,7 @@ __device__ __forceinline__ int ticket_acq_rel(int32_t *p) {
 
 // Exclusive prefix sum of one int per thread over the CTA (kFrontThreads threads) via
 // shared tmp (one int per warp); *total gets the sum. All threads call it.
-__device__ __forceinline__ int ws_scan(int v, int *tmp, int *total) {
+__device__ __forceinline__ int front_scan(int v, int *tmp, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -76,7 +76,7 @@ __device__ __forceinline__ int ws_scan(int v, int *tmp, int *total) {
 
 // The rank k whose items [pos[k], pos[k + 1]) hold item p (pos ascending, pos[U] = W;
 // U when p >= W).
-__device__ __forceinline__ int ws_rank_at(const int *pos, int U, int p) {
+__device__ __forceinline__ int stream_rank_at(const int *pos, int U, int p) {
   int lo = 0, hi = U;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -385,23 +385,22 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
 
 
 // ---------------------------------------------------------------------------
-// Fused step in balanced mode (the attention's balanced plan: more than 19 units or
-// selections above 1024 pages, up to 1024 units) when a unit can have more than
+// Fused step in the attention's workspace mode (more than 19 units with selections
+// above 256 pages, or selections above 1024 pages) when a unit can have more than
 // kFrontSelectMaxCandidates candidates: three launches, each a programmatic dependent
-// of the one before. (With fewer, the front kernel below selects, as in the other
-// modes: two launches.)
+// of the one before. (With fewer, the front kernel above selects: two launches.)
 //   1. step_score_balanced: a persistent grid; the score tiles (64 summary rows) of
 //      every retrieval and dual unit, in unit order, form one stream cut into equal
 //      contiguous shares, one per CTA; a CTA streams its tiles through a ring of nbuf
 //      buffers (the next tiles' bulk copies fly during this tile's dot products, across
 //      units). Every CTA first updates the appended token's sub-block (a1) of a few
 //      units, one unit per warp, while its first copies fly.
-//   2. step_select_kernel: one CTA per unit: a3, the page list, the published count and
-//      a5. Streaming units need no scores and go ahead at once; the others wait for
-//      launch 1 to finish.
-//   3. the attention (balanced plan), which waits per unit for the published count.
+//   2. step_select_kernel: one CTA per unit: a3, the published count and a5. Streaming
+//      units need no scores and go ahead at once; the others wait for launch 1 to
+//      finish.
+//   3. the attention (workspace mode), which waits per unit for the published count.
 // ---------------------------------------------------------------------------
-constexpr int kMaxFrontRing = 3;   // tile buffers of the balanced score kernel, at most
+constexpr int kMaxFrontRing = 3;   // tile buffers of the stream score kernel, at most
 
 // A unit's head configuration, length and geometry for the step kernels.
 struct FrontUnit {
@@ -476,7 +475,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
       mine += n;
     }
     int total;
-    int run = ws_scan(mine, scan_tmp, &total);
+    int run = front_scan(mine, scan_tmp, &total);
     for (int u = u0; u < u1; ++u) {
       const int n = pos[u];
       pos[u] = run;
@@ -499,7 +498,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
   float *dots = reinterpret_cast<float *>(smem + L::off_dots(nbuf));
   auto first_tile = [&](int u) { return max(p0, pos[u]) - pos[u]; };
   auto end_tile = [&](int u) { return min(p1, pos[u + 1]) - pos[u]; };
-  int issue_u = p0 < p1 ? ws_rank_at(pos, U, p0) : U;
+  int issue_u = p0 < p1 ? stream_rank_at(pos, U, p0) : U;
   int issue_t = issue_u < U ? first_tile(issue_u) : 0;
   int comp_u = issue_u, comp_t = issue_t;
   // The issuing unit's summary rows: its first candidate row and the end of its rows.
@@ -612,7 +611,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
   if (!attr_ok) return BS_ERR_CUDA;
   const int units = dims.batch * dims.n_kv_heads;
-  const int mode = attn_mode(units, dims.max_gather_pages_per_unit, dims.kv_dtype);
+  const int mode = attn_mode(units, dims.max_gather_pages_per_unit);
   const bool lists = mode != kModeWorkspace;   // the attention reads page lists
   int pt_cache = lists && dims.max_pages_per_unit <= kPtCacheInts ? dims.max_pages_per_unit : 0;
   size_t front_smem = front_select_bytes(dims.max_blocks_per_unit, dims.max_sel_per_unit, pt_cache);
@@ -622,8 +621,8 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
   }
   const StepWords words = step_words(io.workspace, units);
   int32_t *plist = lists ? words.tickets + attn_counter_floats(units) : nullptr;
-  if (step_selects_apart(units, dims.max_gather_pages_per_unit, dims.kv_dtype, dims.max_blocks_per_unit)) {
-    // 1. balanced scores: the ring of nbuf score tiles, the queries and dot products,
+  if (step_selects_apart(units, dims.max_gather_pages_per_unit, dims.max_blocks_per_unit)) {
+    // 1. scores in equal shares: the ring of nbuf score tiles, the queries and dot products,
     //    then the plan; nbuf 2 or 3, whichever gives more tiles in flight per SM
     //    (preferring more CTAs).
     static const bool sc_ok = cudaFuncSetAttribute(step_score_balanced<D, G>,
@@ -696,7 +695,7 @@ bs_status launch_step_attention(const bs_dims &dims, const bs_kv &kv, const bs_h
   a.out = io.out;
   a.lse = io.lse;
   a.arrivals = words.arrivals;
-  a.records = static_cast<float *>(io.workspace) + attn_records_offset(units, dims.max_gather_pages_per_unit, mode);
+  a.records = static_cast<float *>(io.workspace) + attn_records_offset(units);
   a.plist = plist;
   a.pub = words.pub;
   a.expect = words.expect;

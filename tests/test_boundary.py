@@ -73,18 +73,14 @@ def _ws(units, G, max_gather, kv=B.BS_BF16):
 
 def test_workspace_size_modes():
     """Four int32 words per unit (padded to 16 bytes), then per mode as the header states:
-    cluster mode the fused step's page lists (4 bytes per gathered page); balanced mode
-    the page lists and one split record of G x (d + 4) floats per (unit + CTA), for up
-    to 512 CTAs; workspace mode 32 split records per unit. And the 8 MiB limit of the
+    cluster mode the fused step's page lists (4 bytes per gathered page); workspace mode
+    32 split records of G x (d + 4) floats per unit. And the 8 MiB limit of the
     no-allocation call that follows from it."""
     def counters(u):
         return (4 * u + 3) // 4 * 4 * 4
 
     def plist(u, mg):
         return (u * mg + 3) // 4 * 4 * 4
-
-    def balanced(u, G, mg):
-        return counters(u) + plist(u, mg) + (u + 512) * G * (128 + 4) * 4
 
     def workspace(u, G):
         return counters(u) + u * 32 * G * (128 + 4) * 4
@@ -93,21 +89,19 @@ def test_workspace_size_modes():
     assert _ws(19, 4, 1024) == counters(19) + plist(19, 1024)
     assert _ws(20, 4, 256) == counters(20) + plist(20, 256)         # small selections: cluster
     assert _ws(304, 4, 1024) == counters(304) + plist(304, 1024)    # many units: cluster
-    assert _ws(8, 4, 1025) == balanced(8, 4, 1025)                  # above 1024 pages
-    assert _ws(20, 4, 257) == balanced(20, 4, 257)                  # 20..303 units, larger selections
-    assert _ws(303, 4, 512) == balanced(303, 4, 512)
-    assert _ws(1024, 7, 1025) == balanced(1024, 7, 1025)
+    assert _ws(8, 4, 1025) == workspace(8, 4)                       # above 1024 pages
+    assert _ws(20, 4, 257) == workspace(20, 4)                      # 20..303 units, larger selections
+    assert _ws(303, 7, 512) == workspace(303, 7)
     assert _ws(1025, 4, 512) == counters(1025) + plist(1025, 512)   # many units: cluster
     assert _ws(1025, 4, 2048) == workspace(1025, 4)
-    # fp32 caches keep the cluster / workspace plan
+    # the same rule for fp32 caches
     assert _ws(8, 4, 2048, B.BS_FP32) == workspace(8, 4)
     assert _ws(100, 4, 512, B.BS_FP32) == workspace(100, 4)
     assert _ws(100, 4, 256, B.BS_FP32) == counters(100) + plist(100, 256)
     limit = 8 << 20
-    assert _ws(303, 8, 512) <= limit                                # every balanced launch at 512 pages
-    assert _ws(1024, 4, 1024) <= limit                              # (cluster)
-    assert _ws(708, 4, 2048) <= limit < _ws(709, 4, 2048)
-    assert _ws(500, 8, 2048) <= limit < _ws(501, 8, 2048)
+    assert _ws(124, 4, 2048) <= limit < _ws(125, 4, 2048)          # workspace mode
+    assert _ws(62, 8, 2048) <= limit < _ws(63, 8, 2048)
+    assert _ws(2040, 4, 1024) <= limit < _ws(2041, 4, 1024)        # cluster mode
 
 
 class HostCfg:

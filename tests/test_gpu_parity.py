@@ -226,12 +226,12 @@ def test_parity_full_size(cfg, fused):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("name,cfg,kw", [("cluster-16-units", 5, dict(B=2, T=2040, steps=6)),
                                          ("cluster-32-units", 5, dict(B=4, T=2040, steps=16)),
-                                         ("balanced-32-units", 5, dict(B=4, T=8190, steps=4))])
+                                         ("workspace-32-units", 5, dict(B=4, T=8190, steps=4))])
 @pytest.mark.parametrize("fused", [False, True])
 def test_parity_ed_dma(name, cfg, kw, fused):
     wl = make_workload(cfg, seed=41, **kw)
-    if name.startswith("balanced"):
-        wl.k[:] = 80                    # selections above 256 pages over 32 units: the balanced plan
+    if name.startswith("workspace"):
+        wl.k[:] = 80                    # selections above 256 pages over 32 units: the workspace plan
         wl.k_e[:] = 60
     rep = run_parity(wl, fused=fused, ed_dma=True)
     rep.check()
@@ -263,8 +263,8 @@ def _random_block_logits(layer, rng, sel):
 
 @pytest.mark.parametrize("name,cfg,kw", [("fp32-cluster", 1, {}), ("fp32-workspace", 1, dict(B=24, T=9000)),
                                          ("bf16-cluster", 2, dict(T=4133)),
-                                         ("bf16-balanced", 4, dict(B=6, T_range=(3000, 6000))),
-                                         ("bf16-balanced-1200-pages", 2, dict(T=20000))])
+                                         ("bf16-workspace", 4, dict(B=6, T_range=(3000, 6000))),
+                                         ("bf16-workspace-1200-pages", 2, dict(T=20000))])
 @pytest.mark.parametrize("noalloc", [False, True])
 def test_ed_dma_block_logits_every_plan(name, cfg, kw, noalloc):
     """bs_sparse_decode_attn with random block logits (some -inf, one unit all -inf)
@@ -272,9 +272,9 @@ def test_ed_dma_block_logits_every_plan(name, cfg, kw, noalloc):
     wl = make_workload(cfg, seed=42, **kw)
     if name == "fp32-workspace":
         wl.k[:] = 70                     # ~290 pages per unit over 24 units: the workspace plan
-    if name == "bf16-balanced":
-        wl.k[:] = 80                     # ~330 pages per unit over 24 units: the balanced plan
-    if name == "bf16-balanced-1200-pages":
+    if name == "bf16-workspace":
+        wl.k[:] = 80                     # ~330 pages per unit over 24 units: the workspace plan
+    if name == "bf16-workspace-1200-pages":
         wl.k[4:] = 600                   # above 1024 pages per unit
     layer = PagedLayer(wl)
     layer.prefill()
