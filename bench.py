@@ -632,8 +632,11 @@ def run_ours(args) -> None:
                   for k in per_kernel}
     # The roofline of the timed path: one layer step is the launches of bs_decode_step,
     # each a programmatic dependent of the one before (overlapping), timed as one.
+    # traffic: DRAM bytes of one layer step's kernels (one ncu capture of each on a
+    # small case of this workload, profiles/), only while no library source changed.
+    traffic = _measured_traffic("layer_step", wl.name) if args.path == "fused" else None
     roofline = {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(layer_gbs / peak, 4), "traffic": None,
+                "frac": round(layer_gbs / peak, 4), "traffic": traffic,
                 "kernel": (f"bs_decode_step = {step_kernels(wl, bn.launches_per_layer)} (one layer step; "
                            "the launches overlap through programmatic dependent launch)" if args.path == "fused"
                            else "the five calls of one layer step"),
