@@ -306,7 +306,11 @@ typedef struct {
  * this step's) and writes the set-difference. Launch 2 is the attention, launched as a
  * programmatic dependent: streaming units' pages need no selection and are attended
  * before launch 1 ends; the others wait, bounded, for their unit's published word.
- * Both launches may begin before the work ahead of them in `stream` has finished;
+ * With three launches: launch 1 scores the tiles of all units as one stream in equal
+ * shares over a persistent grid; launch 2 runs one 1024-thread CTA per unit that
+ * updates a1, waits for launch 1 (streaming units do not wait), selects, publishes and
+ * writes the set-difference; launch 3 is the attention as above.
+ * The launches may begin before the work ahead of them in `stream` has finished;
  * before waiting for it they read only the per-unit head configuration (cfg arrays),
  * so those must not be written by the kernel immediately before this call. Everything
  * else is read after that work has finished. Requires max_sel_per_unit <= 4096.

@@ -393,11 +393,10 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
 //      every retrieval and dual unit, in unit order, form one stream cut into equal
 //      contiguous shares, one per CTA; a CTA streams its tiles through a ring of nbuf
 //      buffers (the next tiles' bulk copies fly during this tile's dot products, across
-//      units). Every CTA first updates the appended token's sub-block (a1) of a few
-//      units, one unit per warp, while its first copies fly.
-//   2. step_select_kernel: one CTA per unit: a3, the published count and a5. Streaming
-//      units need no scores and go ahead at once; the others wait for launch 1 to
-//      finish.
+//      units).
+//   2. step_select_kernel: one CTA per unit: a1 (one warp, while the others wait), a3,
+//      the published count and a5. Streaming units need no scores and go ahead at
+//      once; the others wait for launch 1 to finish.
 //   3. the attention (workspace mode), which waits per unit for the published count.
 // ---------------------------------------------------------------------------
 constexpr int kMaxFrontRing = 3;   // tile buffers of the stream score kernel, at most
@@ -437,15 +436,6 @@ __device__ __forceinline__ FrontUnit load_front_unit(const bs_dims &dims, const 
     if (f.cls != BS_STREAMING && f.ge.c_hi > f.ge.c_lo) f.tiles = score_tiles(f.ge);
   }
   return f;
-}
-
-// a1 of unit u by the calling warp (a function of its own, so that its registers do
-// not weigh on the score loop around it).
-template <int D>
-__device__ __noinline__ void step_a1_unit(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &cfg,
-                                          const bs_step_io &io, int u) {
-  const FrontUnit f = load_front_unit(dims, kv, cfg, io, u);
-  if (f.code == BS_OK) unit_summary_update<D>(dims, kv, io, u, f.s, f.T, f.off, io.dev_status);
 }
 
 template <int D, int G>
@@ -531,9 +521,6 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
   };
   for (int i = 0; i < nbuf; ++i) issue_next(i);
 
-  // ---- a1 of units c, c + P, ... (one warp each), while the first copies fly ----------
-  for (int u = c + warp * P; u < U; u += P * (kFrontThreads / 32)) step_a1_unit<D>(dims, kv, cfg, io, u);
-
   int q_u = -1;
   Geom cge;
   for (int n_done = 0; comp_u < U && pos[comp_u] < p1; ++n_done) {
@@ -575,6 +562,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
 // others wait for the score kernel (and everything before it) to finish.
 constexpr int kStepSelThreads = 1024;   // at most 8 candidates per thread in registers up to 8192
 
+template <int D>
 __global__ void __launch_bounds__(kStepSelThreads) step_select_kernel(bs_dims dims, bs_kv kv, bs_head_cfg cfg,
                                                                     bs_step_io io, StepWords words, int32_t *plist,
                                                                     int pt_cache_ints) {
@@ -583,6 +571,10 @@ __global__ void __launch_bounds__(kStepSelThreads) step_select_kernel(bs_dims di
   const int u = blockIdx.x;
   pdl_trigger_front();   // the attention may start launching
   const FrontUnit f = load_front_unit(dims, kv, cfg, io, u);
+  // a1 by warp 0 while the others wait for the scores: the sub-block holding the
+  // appended token lies in the always-forced tail block, which no score of this step
+  // reads, and its K pages were written before the score kernel started.
+  if (f.code == BS_OK && threadIdx.x < 32) unit_summary_update<D>(dims, kv, io, u, f.s, f.T, f.off, io.dev_status);
   if (f.code != BS_OK || f.cls != BS_STREAMING) pdl_wait_front();
   if (f.code != BS_OK) {
     unit_error_publish(dims, io, words, u, f.code);
@@ -628,7 +620,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
     static const bool sc_ok = cudaFuncSetAttribute(step_score_balanced<D, G>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess &&
-                              cudaFuncSetAttribute(step_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              cudaFuncSetAttribute(step_select_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(kFrontMaxSmem)) == cudaSuccess;
     if (!sc_ok) return BS_ERR_CUDA;
     int dev = 0, sms = 0;
@@ -657,7 +649,7 @@ bs_status launch_step(const bs_dims &dims, const bs_kv &kv, const bs_head_cfg &c
                   kv, cfg, io, reduce, best_plan, best_nbuf) != cudaSuccess)
       return BS_ERR_CUDA;
     // 2. selection, one CTA per unit.
-    if (launch_ex(step_select_kernel, dim3(units), kStepSelThreads, front_smem, cs, 0, true, dims, kv, cfg, io, words,
+    if (launch_ex(step_select_kernel<D>, dim3(units), kStepSelThreads, front_smem, cs, 0, true, dims, kv, cfg, io, words,
                   plist, pt_cache) != cudaSuccess)
       return BS_ERR_CUDA;
     // 3. attention.
