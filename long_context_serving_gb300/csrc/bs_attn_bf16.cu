@@ -28,7 +28,7 @@ bs_status launch_modes(const AttnArgs &a, bool step, const CUtensorMap &tk, cons
   if (!attrs_ok) return BS_ERR_CUDA;
   const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit) == kModeCluster;
   const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
-  const dim3 grid(splits, units);
+  const dim3 grid = cluster ? dim3(splits, units) : dim3(units, splits);   // (workspace mode: unit-major)
   const cudaError_t e =
       launch_ex(kernel, grid, kMmaThreads, kSmem, cs, cluster && splits > 1 ? splits : 0, step, a, tk, tv, step, cluster);
   return e == cudaSuccess ? BS_OK : BS_ERR_CUDA;

@@ -50,6 +50,21 @@
 namespace bsi {
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// A CTA's unit and split. The grid is (splits, units) in cluster mode, where a unit's
+// splits form one cluster along x, and (units, splits) in workspace mode, so that every
+// unit's first split is dispatched before any unit's second: in the fused step a unit
+// whose selection is published early does not queue behind the splits of units still
+// being selected.
+__device__ __forceinline__ int attn_unit_id(bool in_cluster) {
+  return static_cast<int>(in_cluster ? blockIdx.y : blockIdx.x);
+}
+__device__ __forceinline__ int attn_split_id(bool in_cluster) {
+  return static_cast<int>(in_cluster ? blockIdx.x : blockIdx.y);
+}
+__device__ __forceinline__ int attn_n_splits(bool in_cluster) {
+  return static_cast<int>(in_cluster ? gridDim.x : gridDim.y);
+}
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kSelPreload = 512;  // selection entries staged in shared memory
 constexpr int kMmaThreads = 128;  // bf16 path: 4 warps, one page each per stage
@@ -138,7 +153,7 @@ __device__ UnitBlocks load_unit_blocks(const AttnArgs &a, int u, int32_t *sel_sm
   const int32_t *sel_idx = a.sel_idx, *sel_cnt = a.sel_cnt, *plist = a.plist;
   int32_t *st = a.st;
   __shared__ int sh_cnt;
-  const int tid = threadIdx.x, split = blockIdx.x;
+  const int tid = threadIdx.x, split = attn_split_id(in_cluster);
   const int b = u / dims.n_kv_heads;
   UnitBlocks ub;
   ub.T = kv.seq_lens[b];
@@ -275,7 +290,7 @@ __device__ __forceinline__ void write_normalised(float4 o, float m, float l, flo
 // unnormalised output [G][D] (fp32, shared), `m_sm`/`l_sm` its per-head max (log2
 // units) and sum. A launch with one split per unit writes out/lse; otherwise every
 // launched split (an idle one with an empty state) publishes its record and takes a
-// ticket, and the last of the gridDim.x splits merges all records in split order and,
+// ticket, and the last of the unit's splits merges all records in split order and,
 // in the fused step, advances the unit's epoch (every split has read it by then).
 // `scratch` needs 3 * kMaxG * kAttnMaxSplits floats of shared memory. All NT threads
 // call it.
@@ -287,8 +302,9 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
   constexpr int REC = attn_record_floats(D);
   __shared__ int is_last;
   __shared__ float ML[2][kMaxG];
-  const int tid = threadIdx.x, split = blockIdx.x;
-  if (gridDim.x == 1) {
+  // (workspace mode: the grid is (units, splits), attn_split_id)
+  const int tid = threadIdx.x, split = attn_split_id(false);
+  if (attn_n_splits(false) == 1) {
     for (int i = tid; i < G * QD; i += NT) {
       const int h = i / QD, dq = i % QD;
       write_normalised(reinterpret_cast<const float4 *>(o_sm + h * D)[dq], m_sm[h], l_sm[h], out + (orow0 + h) * D,
@@ -309,7 +325,7 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
   // Publish the record and take an arrival ticket: the CTA barrier orders every
   // thread's record writes before thread 0's release; the last split acquires.
   __syncthreads();
-  const int ns = static_cast<int>(gridDim.x);
+  const int ns = attn_n_splits(false);
   if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == ns - 1);
   __syncthreads();
   if (!is_last) return;
@@ -704,7 +720,7 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   const bs_dims &dims = a.dims;
   int32_t *st = a.st;
 
-  const int u = blockIdx.y, split = blockIdx.x;
+  const int u = attn_unit_id(in_cluster), split = attn_split_id(in_cluster);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
@@ -893,7 +909,7 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
   __shared__ float slot_bias[2][kStagePages];   // log2 units, 0 without biases
   __shared__ float ml_sm[2][kMaxG];
 
-  const int u = blockIdx.y, split = blockIdx.x;
+  const int u = attn_unit_id(in_cluster), split = attn_split_id(in_cluster);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
