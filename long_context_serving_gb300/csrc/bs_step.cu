@@ -298,13 +298,24 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   score_bars_init(bars, nbuf);
   __syncthreads();
   pdl_trigger_front();  // the attention may start launching
-  // Start the copies of this CTA's first tiles before reading the length; every path
-  // below waits for whatever is in flight (drain) before returning or reusing memory.
+  // A CTA starts the copies of its first tiles before reading the length when it takes
+  // one tile (short, latency-bound launches) or is its unit's first; the later CTAs of
+  // multi-tile launches read it first and copy only rows of the unit's candidates (with
+  // unequal lengths in a batch, their tiles often lie past them). Every path below waits
+  // for whatever is in flight (drain) before returning or reusing memory.
   const bool spec = scored && off >= 0 && off % 4 == 0;
   const float *summ = io.summaries + (spec ? off : 0);
+  int64_t first_end = rows;
+  if (cj > 0 && tpc > 1 && spec) {
+    const int T0 = kv.seq_lens[b];
+    if (T0 >= 1) {
+      const int64_t cand_end = static_cast<int64_t>(unit_geom(T0, g, s, sink, local).c_hi) * (g / s);
+      first_end = min(static_cast<int64_t>(rows), cand_end);
+    }
+  }
   int inflight[2] = {0, 0}, uses[2] = {0, 0};
   for (int i = 0; i < nbuf && i < tpc; ++i)
-    inflight[i] = score_copy<D>(summ, spec ? tile_row(t0 + i) : -1, rows, smem + i * L::kTileBytes, &bars[i]);
+    inflight[i] = score_copy<D>(summ, spec ? tile_row(t0 + i) : -1, first_end, smem + i * L::kTileBytes, &bars[i]);
   // The queries too: their loads fly beside the copies and the length's.
   const size_t qbase = (static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G) * D;
   const void *qrow = dims.q_dtype == BS_BF16
@@ -357,7 +368,8 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
       score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qs, dots, ge, t0 + kk, reduce,
                           n_rows, score_row);
       if (kk + nbuf < my_tiles)
-        inflight[bi] = score_copy<D>(summ, tile_row(t0 + kk + nbuf), rows, smem + bi * L::kTileBytes, &bars[bi]);
+        inflight[bi] = score_copy<D>(summ, tile_row(t0 + kk + nbuf), static_cast<int64_t>(ge.c_hi) * (g / s),
+                                     smem + bi * L::kTileBytes, &bars[bi]);
     }
   }
   if (!drain()) return;
