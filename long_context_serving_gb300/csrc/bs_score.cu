@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(bs_dims dims, cons
   float *qs = reinterpret_cast<float *>(smem_raw + L::off_q(nbuf));
   float *dots = reinterpret_cast<float *>(smem_raw + L::off_dots(nbuf));
   score_load_q<D, G>(qs, qrow, dims.q_dtype);
+  ScoreQ<D, G> qf;
   for (int kk = 0; kk < my_tiles; ++kk) {
     const int bi = kk % nbuf;
     const int n_rows = inflight[bi];
@@ -90,10 +91,13 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(bs_dims dims, cons
       for (int i = 0; i < nbuf; ++i) score_wait(&bars[i], static_cast<uint32_t>(uses[i] & 1), inflight[i], st);
       return;
     }
-    score_compute<D, G>(reinterpret_cast<const float *>(smem_raw + bi * L::kTileBytes), qs, dots, ge, t0 + kk,
-                        reduce, n_rows, row_out);
-    if (kk + nbuf < my_tiles)
-      inflight[bi] = score_copy<D>(summ_u, tile_row(t0 + kk + nbuf), row_end, smem_raw + bi * L::kTileBytes, &bars[bi]);
+    if (kk == 0) qf = score_qfrag<D, G>(qs);   // (the wait above was a CTA barrier)
+    score_compute<D, G>(reinterpret_cast<const float *>(smem_raw + bi * L::kTileBytes), qf, dots, ge, t0 + kk,
+                        reduce, n_rows, row_out, [&] {
+                          if (kk + nbuf < my_tiles)
+                            inflight[bi] = score_copy<D>(summ_u, tile_row(t0 + kk + nbuf), row_end,
+                                                         smem_raw + bi * L::kTileBytes, &bars[bi]);
+                        });
   }
 }
 

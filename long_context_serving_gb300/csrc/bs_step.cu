@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
   const int my_tiles = (cls != BS_STREAMING && ge.c_hi > ge.c_lo) ? max(0, min(tpc, n_tiles - t0)) : 0;
   if (my_tiles > 0) {
     float *dots = reinterpret_cast<float *>(smem + L::off_dots(nbuf));
+    ScoreQ<D, G> qf;
     for (int kk = 0; kk < my_tiles; ++kk) {
       const int bi = kk % nbuf;
       const int n_rows = inflight[bi];
@@ -365,11 +366,14 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_front_kernel(bs_dims di
         drain();
         return;
       }
-      score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qs, dots, ge, t0 + kk, reduce,
-                          n_rows, score_row);
-      if (kk + nbuf < my_tiles)
-        inflight[bi] = score_copy<D>(summ, tile_row(t0 + kk + nbuf), static_cast<int64_t>(ge.c_hi) * (g / s),
-                                     smem + bi * L::kTileBytes, &bars[bi]);
+      if (kk == 0) qf = score_qfrag<D, G>(qs);   // (the wait above was a CTA barrier)
+      score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qf, dots, ge, t0 + kk, reduce,
+                          n_rows, score_row, [&] {
+                            if (kk + nbuf < my_tiles)
+                              inflight[bi] = score_copy<D>(summ, tile_row(t0 + kk + nbuf),
+                                                           static_cast<int64_t>(ge.c_hi) * (g / s),
+                                                           smem + bi * L::kTileBytes, &bars[bi]);
+                          });
     }
   }
   if (!drain()) return;
@@ -535,6 +539,7 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
 
   int q_u = -1;
   Geom cge;
+  ScoreQ<D, G> qf;
   for (int n_done = 0; comp_u < U && pos[comp_u] < p1; ++n_done) {
     const int bi = n_done % nbuf;
     if (comp_u != q_u) {   // a new unit: its geometry and its queries (scaled) into shared memory
@@ -548,15 +553,16 @@ __global__ void __launch_bounds__(kFrontThreads, 2) step_score_balanced(bs_dims 
                              : static_cast<const void *>(static_cast<const float *>(io.q) + qbase);
       score_load_q<D, G>(qs, qrow, dims.q_dtype);
       __syncthreads();
+      qf = score_qfrag<D, G>(qs);
     }
     const int n_rows = inflight[bi];
     const bool ok = score_wait(&bars[bi], static_cast<uint32_t>(uses[bi] & 1), n_rows, st);
     if (n_rows > 0) ++uses[bi];
     inflight[bi] = 0;
     if (!ok) break;   // (reported) a copy that never landed: no more tiles
-    score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qs, dots, cge, comp_t, reduce,
-                        n_rows, io.scores + static_cast<size_t>(comp_u) * dims.max_blocks_per_unit);
-    issue_next(bi);
+    score_compute<D, G>(reinterpret_cast<const float *>(smem + bi * L::kTileBytes), qf, dots, cge, comp_t, reduce,
+                        n_rows, io.scores + static_cast<size_t>(comp_u) * dims.max_blocks_per_unit,
+                        [&] { issue_next(bi); });
     if (++comp_t >= end_tile(comp_u)) {
       do {
         ++comp_u;
