@@ -20,17 +20,18 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnArgs a, const
 template <int D, int G>
 bs_status launch_modes(const AttnArgs &a, bool step, const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t cs) {
   const int units = a.dims.batch * a.dims.n_kv_heads;
-  constexpr int kSmem = MmaLayout<D>::kBytes + kSmemAlignSlack;
+  constexpr int kSmemMax = MmaLayout<D>::bytes(MmaLayout<D>::kRingMax) + kSmemAlignSlack;
   auto kernel = attn_mma_kernel<D, G>;
   static const bool attrs_ok =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) == cudaSuccess &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax) == cudaSuccess &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
   if (!attrs_ok) return BS_ERR_CUDA;
   const bool cluster = attn_mode(units, a.dims.max_gather_pages_per_unit) == kModeCluster;
+  const int smem = MmaLayout<D>::bytes(attn_mma_ring(cluster)) + kSmemAlignSlack;
   const int splits = attn_grid_splits(units, a.dims.max_gather_pages_per_unit, attn_target_ctas());
   const dim3 grid = cluster ? dim3(splits, units) : dim3(units, splits);   // (workspace mode: unit-major)
   const cudaError_t e =
-      launch_ex(kernel, grid, kMmaThreads, kSmem, cs, cluster && splits > 1 ? splits : 0, step, a, tk, tv, step, cluster);
+      launch_ex(kernel, grid, kMmaThreads, smem, cs, cluster && splits > 1 ? splits : 0, step, a, tk, tv, step, cluster);
   return e == cudaSuccess ? BS_OK : BS_ERR_CUDA;
 }
 

@@ -10,7 +10,8 @@
 // a multiple of 4 pages. One CTA per (split, unit):
 //   * the unit's page-table row is pulled into L2 while the selection count and row are
 //     read into shared memory; warp 0 resolves the split's pages 32 at a time and stages
-//     them into a ring of 4-page stages (three deep for bf16, two for fp32) with TMA
+//     them into a ring of 4-page stages (for bf16 three deep in cluster mode and two
+//     in workspace mode, with three CTAs per SM; two for fp32) with TMA
 //     copies that complete an mbarrier with their byte count;
 //   * bf16 caches (attn_split_mma, 4 warps): each warp takes one 16-token page per
 //     stage. Pages arrive through a tiled tensor map with 128-byte swizzle, so
@@ -480,20 +481,24 @@ __device__ void cluster_merge(size_t orow0, const float *o_sm, const float *m_sm
 // ===========================================================================
 template <int D>
 struct MmaLayout {
-  static constexpr int kRing = 3;                      // stages in flight
+  static constexpr int kRingMax = 3;                   // stages in flight, at most
   static constexpr int kHalves = D / 64;               // 128-byte-wide column halves of a row
   static constexpr int kHalfBytes = kPage * 128;       // 16 rows x 128 B = 2 KiB (swizzle atom x2)
   static constexpr int kPageBytes = kHalves * kHalfBytes;
   static constexpr int kStageKV = kStagePages * kPageBytes;  // K (or V) of one stage
   static constexpr int kBufBytes = 2 * kStageKV;              // K then V
-  static constexpr int kOffSel = kRing * kBufBytes;
-  static constexpr int kOffQlo = kOffSel + kSelPreload * 4;    // [D/16][2][32] remainder fragments
-  static constexpr int kBytes = kOffQlo + (D / 16) * 2 * 32 * 4;
+  // `ring` stage buffers, then the staged selection entries.
+  __host__ __device__ static constexpr int off_sel(int ring) { return ring * kBufBytes; }
+  __host__ __device__ static constexpr int bytes(int ring) { return off_sel(ring) + kSelPreload * 4; }
   // After the last stage: warp states [4][8][D] and (m, l) reuse buffer 0; the merge's
   // scratch reuses buffer 1.
   static_assert(4 * kMaxG * D * 4 + 2 * 4 * kMaxG * 4 <= kBufBytes, "combine scratch");
   static_assert(3 * kMaxG * kAttnMaxSplits * 4 <= kBufBytes, "merge scratch");
 };
+
+// Stages in flight per CTA: three in cluster mode; two in workspace mode, where a third
+// CTA per SM (more splits resident while units wait for their selections) pays more.
+__host__ __device__ constexpr int attn_mma_ring(bool cluster) { return cluster ? 3 : 2; }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
   asm volatile(
@@ -713,10 +718,10 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   using L = MmaLayout<D>;
   constexpr int NT = kMmaThreads;
   constexpr int KSTEPS = D / 16;
-  constexpr int R = L::kRing;
-  __shared__ uint64_t bars[R];
-  __shared__ int slot_valid[R][kStagePages];
-  __shared__ float slot_bias[R][kStagePages];   // log2 units, 0 without biases
+  const int R = attn_mma_ring(in_cluster);
+  __shared__ uint64_t bars[L::kRingMax];
+  __shared__ int slot_valid[L::kRingMax][kStagePages];
+  __shared__ float slot_bias[L::kRingMax][kStagePages];   // log2 units, 0 without biases
   const bs_dims &dims = a.dims;
   int32_t *st = a.st;
 
@@ -724,7 +729,7 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
-  int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
+  int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::off_sel(R));
 
   prefetch_page_row<NT>(dims, a.kv, a.cfg, a.plist, u, in_step);
   const UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
@@ -738,7 +743,6 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   const int32_t *pt = a.kv.page_table + static_cast<size_t>(u) * dims.max_pages_per_unit;
 
   if (tid == 0) {
-#pragma unroll
     for (int i = 0; i < R; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
