@@ -12,9 +12,10 @@ __global__ void __launch_bounds__(kMmaThreads) attn_mma_kernel(AttnArgs a, const
                                                                bool cluster) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   if (step) pdl_launch_dependents();
-  attn_split_mma<D, G>(a, &tmk, &tmv, align_smem_1024(smem_raw), step, cluster);
-  // In the fused step, finish only after the selection kernel has.
-  if (step) pdl_wait();
+  const bool took_part = attn_split_mma<D, G>(a, &tmk, &tmv, align_smem_1024(smem_raw), step, cluster);
+  // In the fused step, finish only after the selection kernel has (a split that took no
+  // part leaves at once: split 0 of every unit takes part, so the grid still does).
+  if (step && took_part) pdl_wait();
 }
 
 template <int D, int G>

@@ -10,8 +10,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(kFfmaThreads) attn_ffma_kernel(AttnArgs a, bool step, bool cluster) {
   extern __shared__ __align__(128) unsigned char smem[];
   if (step) pdl_launch_dependents();
-  attn_split_ffma<D, G>(a, smem, step, cluster);
-  if (step) pdl_wait();
+  const bool took_part = attn_split_ffma<D, G>(a, smem, step, cluster);
+  if (step && took_part) pdl_wait();   // (as in the bf16 kernel)
 }
 
 template <int D, int G>

@@ -223,6 +223,40 @@ __device__ UnitBlocks load_unit_blocks(const AttnArgs &a, int u, int32_t *sel_sm
   return ub;
 }
 
+// Splits of unit u that take part in the fused step's workspace-mode attention, from the
+// head configuration and the length alone (every split of the unit computes the same
+// number before any wait): a selection holds the forced blocks (sink, local window,
+// tail) and at most k others, so its pages are at most min(n_blk, |F| + k) * g/16, and
+// with splits of 32 pages (selections up to 1024 pages) the split count grows with the
+// pages. The splits past it can hold no page: they leave at once instead of holding an
+// SM slot until the unit's selection is published. Any other case: every launched split.
+__device__ __forceinline__ int step_ws_splits(const AttnArgs &a, int u, int launched) {
+  const bs_dims &dims = a.dims;
+  if (attn_min_split_pages(dims.max_gather_pages_per_unit) != kMidSplitPages) return launched;
+  const bs_head_cfg &cfg = a.cfg;
+  const int cls = cfg.cls[u], g = cfg.block_tokens[u], s = cfg.sub_tokens[u], k = cfg.k_total[u];
+  const int sink = cfg.sink_tokens[u], local = cfg.local_tokens[u];
+  if (!unit_cfg_ok(cls, g, s, k, cfg.k_evict[u], sink, local)) return launched;
+  const int T = a.kv.seq_lens[u / dims.n_kv_heads];
+  if (T < 1) return launched;
+  const Geom ge = unit_geom(T, g, s, sink, local);
+  const int n_forced = ge.n_sink + (ge.n_blk - max(ge.local_lo, ge.n_sink));
+  const long long blocks =
+      cls == BS_STREAMING ? n_forced : min(static_cast<long long>(ge.n_blk), static_cast<long long>(n_forced) + k);
+  const long long pages = min(blocks * (g / kPage), static_cast<long long>(dims.max_gather_pages_per_unit));
+  const int n = static_cast<int>((pages + kMidSplitPages - 1) / kMidSplitPages);
+  return max(1, min(launched, n));
+}
+
+// A selection with more splits than take part would lose pages: it is reported
+// (BS_ERR_DEVICE_BOUNDS) and the unit attends nothing rather than part of it.
+__device__ __forceinline__ void check_split_bound(UnitBlocks &ub, int n_part, int split, int32_t *st) {
+  if (ub.pg.n_split > n_part) {
+    if (split == 0 && threadIdx.x == 0) report(st, BS_ERR_DEVICE_BOUNDS);
+    ub.ok = false;
+  }
+}
+
 // Resolves page slot `lane` (< kStagePages) of a stage: returns the physical page and
 // the number of valid tokens in it (0 for an empty or out-of-range slot). blk_out (may
 // be null) receives the page's block index, -1 for an empty slot.
@@ -289,23 +323,24 @@ __device__ __forceinline__ void write_normalised(float4 o, float m, float l, flo
 
 // Epilogue of the workspace mode, shared by both paths. `o_sm` holds this split's
 // unnormalised output [G][D] (fp32, shared), `m_sm`/`l_sm` its per-head max (log2
-// units) and sum. A launch with one split per unit writes out/lse; otherwise every
-// launched split (an idle one with an empty state) publishes its record and takes a
-// ticket, and the last of the unit's splits merges all records in split order and,
-// in the fused step, advances the unit's epoch (every split has read it by then).
+// units) and sum. With one taking part (`ns`, the splits of the unit that take part:
+// every launched one, or step_ws_splits in the fused step) it writes out/lse; otherwise
+// every split taking part (an idle one with an empty state) publishes its record and
+// takes a ticket, and the last of them merges the records in split order and, in the
+// fused step, advances the unit's epoch (every split taking part has read it by then).
 // `scratch` needs 3 * kMaxG * kAttnMaxSplits floats of shared memory. All NT threads
 // call it.
 template <int NT, int D, int G>
 __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const float *o_sm, const float *m_sm,
                              const float *l_sm, int32_t *arrivals, float *ws, float *out, float *lse, float *scratch,
-                             int32_t *expect) {
+                             int32_t *expect, int ns) {
   constexpr int QD = D / 4;
   constexpr int REC = attn_record_floats(D);
   __shared__ int is_last;
   __shared__ float ML[2][kMaxG];
   // (workspace mode: the grid is (units, splits), attn_split_id)
   const int tid = threadIdx.x, split = attn_split_id(false);
-  if (attn_n_splits(false) == 1) {
+  if (ns == 1) {
     for (int i = tid; i < G * QD; i += NT) {
       const int h = i / QD, dq = i % QD;
       write_normalised(reinterpret_cast<const float4 *>(o_sm + h * D)[dq], m_sm[h], l_sm[h], out + (orow0 + h) * D,
@@ -326,7 +361,6 @@ __device__ void finish_split(const UnitBlocks &ub, int u, size_t orow0, const fl
   // Publish the record and take an arrival ticket: the CTA barrier orders every
   // thread's record writes before thread 0's release; the last split acquires.
   __syncthreads();
-  const int ns = attn_n_splits(false);
   if (tid == 0) is_last = (atomic_add_acq_rel_gpu(arrivals + u, 1) == ns - 1);
   __syncthreads();
   if (!is_last) return;
@@ -712,8 +746,9 @@ __device__ __forceinline__ void add_warp_o(const float (&o)[D / 16][4], const fl
     }
 }
 
+// Returns false for a split that took no part (it left at once; see step_ws_splits).
 template <int D, int G>
-__device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv, unsigned char *smem,
+__device__ bool attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const CUtensorMap *tmv, unsigned char *smem,
                                bool in_step, bool in_cluster) {
   using L = MmaLayout<D>;
   constexpr int NT = kMmaThreads;
@@ -730,12 +765,16 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::off_sel(R));
+  const int n_part = in_step && !in_cluster ? step_ws_splits(a, u, attn_n_splits(false)) : attn_n_splits(in_cluster);
+  if (split >= n_part) return false;
 
   prefetch_page_row<NT>(dims, a.kv, a.cfg, a.plist, u, in_step);
-  const UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
-  // Every launched split of the unit takes part to the end (an idle one with an empty
-  // state): the merge needs all CTAs of a cluster, and in workspace mode the last split
-  // to arrive merges, after every split of the unit has read the unit's words.
+  UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
+  check_split_bound(ub, n_part, split, st);
+  // Every split taking part stays to the end (an idle one with an empty state): the
+  // merge needs all CTAs of a cluster (all launched ones take part there), and in
+  // workspace mode the last split to arrive merges, after every split taking part has
+  // read the unit's words.
   const int n_pages = ub.ok ? ub.pg.n_pages : 0;
   const int gp0 = min(split * ub.pg.pps, n_pages);
   const int gp1 = min(gp0 + ub.pg.pps, n_pages);
@@ -874,8 +913,9 @@ __device__ void attn_split_mma(const AttnArgs &a, const CUtensorMap *tmk, const 
     if (ub.polled && split == 0 && tid == 0) a.expect[u] = ub.epoch;
   } else {
     finish_split<NT, D, G>(ub, u, orow0, osum, mfin, lfin, a.arrivals, a.records, a.out, a.lse,
-                           reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4), a.expect);
+                           reinterpret_cast<float *>(smem + L::kBufBytes + G * D * 4), a.expect, n_part);
   }
+  return true;
 }
 
 // ===========================================================================
@@ -898,8 +938,9 @@ struct FfmaLayout {
   static_assert(2 * kStageBytes >= 3 * kMaxG * kAttnMaxSplits * 4, "merge scratch must fit in the V stages");
 };
 
+// Returns false for a split that took no part (it left at once; see step_ws_splits).
 template <int D, int G>
-__device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_step, bool in_cluster) {
+__device__ bool attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_step, bool in_cluster) {
   using L = FfmaLayout<D, G>;
   const bs_dims &dims = a.dims;
   const bs_kv &kv = a.kv;
@@ -918,10 +959,13 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
   const int b = u / dims.n_kv_heads, hk = u % dims.n_kv_heads;
   const size_t orow0 = static_cast<size_t>(b) * dims.n_q_heads + static_cast<size_t>(hk) * G;
   int32_t *sel_sm = reinterpret_cast<int32_t *>(smem + L::kOffSel);
+  const int n_part = in_step && !in_cluster ? step_ws_splits(a, u, attn_n_splits(false)) : attn_n_splits(in_cluster);
+  if (split >= n_part) return false;
 
   prefetch_page_row<NT>(dims, kv, a.cfg, a.plist, u, in_step);
-  const UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
-  // Every launched split takes part to the end (see attn_split_mma).
+  UnitBlocks ub = load_unit_blocks<NT>(a, u, sel_sm, in_step, in_cluster);
+  check_split_bound(ub, n_part, split, st);
+  // Every split taking part stays to the end (see attn_split_mma).
   const int n_pages = ub.ok ? ub.pg.n_pages : 0;
   const int gp0 = min(split * ub.pg.pps, n_pages);
   const int gp1 = min(gp0 + ub.pg.pps, n_pages);
@@ -1108,8 +1152,9 @@ __device__ void attn_split_ffma(const AttnArgs &a, unsigned char *smem, bool in_
     if (ub.polled && split == 0 && tid == 0) a.expect[u] = ub.epoch;
   } else {
     finish_split<NT, D, G>(ub, u, orow0, osum, ml_sm[0], ml_sm[1], a.arrivals, a.records, a.out, a.lse,
-                           reinterpret_cast<float *>(smem + 2 * L::kStageBytes), a.expect);
+                           reinterpret_cast<float *>(smem + 2 * L::kStageBytes), a.expect, n_part);
   }
+  return true;
 }
 
 }  // namespace bsi
