@@ -226,10 +226,11 @@ __device__ UnitBlocks load_unit_blocks(const AttnArgs &a, int u, int32_t *sel_sm
 // Splits of unit u that take part in the fused step's workspace-mode attention, from the
 // head configuration and the length alone (every split of the unit computes the same
 // number before any wait): a selection holds the forced blocks (sink, local window,
-// tail) and at most k others, so its pages are at most min(n_blk, |F| + k) * g/16, and
-// with splits of 32 pages (selections up to 1024 pages) the split count grows with the
-// pages. The splits past it can hold no page: they leave at once instead of holding an
-// SM slot until the unit's selection is published. Any other case: every launched split.
+// tail) and at most k others, so its pages are at most min(n_blk, |F| + k) * g/16; with
+// selections up to 1024 pages every split but the last holds at least kMidSplitPages
+// pages, so ceil(pages / kMidSplitPages) bounds the split count. The splits past it can
+// hold no page: they leave at once instead of holding an SM slot until the unit's
+// selection is published. Any other case: every launched split.
 __device__ __forceinline__ int step_ws_splits(const AttnArgs &a, int u, int launched) {
   const bs_dims &dims = a.dims;
   if (attn_min_split_pages(dims.max_gather_pages_per_unit) != kMidSplitPages) return launched;

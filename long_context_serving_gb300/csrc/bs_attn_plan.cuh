@@ -39,7 +39,8 @@ __host__ __device__ inline StepWords step_words(void *workspace, size_t units) {
   return StepWords{w, w + units, w + 2 * units, w + 3 * units};
 }
 
-constexpr int kMidSplitPages = 32;   // workspace mode below 1024 pages: pages per split, at least
+constexpr int kMidSplitPages = 24;     // workspace mode up to 1024 pages: pages per split, at least
+constexpr int kClusterSmallPages = 256; // cluster mode for any unit count up to this selection
 constexpr int kClusterUnitsMax = 19; // cluster mode while units x 16 splits fit one wave of ~304 CTAs ...
 constexpr int kManyUnits = 304;      // ... or once the units alone fill it (then one split each)
 
@@ -49,15 +50,16 @@ constexpr int kManyUnits = 304;      // ... or once the units alone fill it (the
 //              cluster and merge through distributed shared memory; every unit has the
 //              same number of splits;
 //   workspace: the rest (selections above 1024 pages, or 20..303 units with selections
-//              that may exceed 8 x 32 pages, whose page counts can then differ a lot
+//              that may exceed 256 pages, whose page counts can then differ a lot
 //              between units): each unit's splits are sized by its own pages (at least
-//              32 per split, so a long unit gets more splits), up to 32, and merge
+//              24 per split up to 1024 pages, 4 beyond, so a long unit gets more
+//              splits), up to 32, and merge
 //              through records in the workspace.
 enum AttnMode { kModeCluster = 0, kModeWorkspace = 1 };
 
 __host__ __device__ inline bool attn_cluster_mode(int units, int max_gather_pages) {
   if (max_gather_pages > kClusterMaxPages) return false;
-  return units <= kClusterUnitsMax || units >= kManyUnits || max_gather_pages <= 8 * kMidSplitPages;
+  return units <= kClusterUnitsMax || units >= kManyUnits || max_gather_pages <= kClusterSmallPages;
 }
 
 __host__ __device__ inline int attn_mode(int units, int max_gather_pages) {
