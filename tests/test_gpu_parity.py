@@ -92,6 +92,20 @@ def test_parity_few_splits_per_unit(B, fused):
     rep.check()
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_parity_workspace_split_bounds(fused):
+    """The workspace plan (24 units, selections above 256 pages) with units whose head
+    configuration bounds them to 1, 3, 8 and 14 splits: in the fused step only those
+    splits take part, and a unit bounded to one split writes its output without a merge."""
+    wl = make_workload(4, seed=21, B=6, T_range=(3000, 6000), steps=2)
+    wl.k[:] = 80
+    wl.k[0::3] = 1
+    wl.sink[0::3] = 0
+    wl.k[1::3] = 10
+    rep = run_parity(wl, fused=fused)
+    rep.check()
+
+
 @pytest.mark.parametrize("T", [1, 17, 40])
 @pytest.mark.parametrize("fused", [False, True])
 def test_parity_tiny_lengths(T, fused):
