@@ -209,9 +209,12 @@ bs_status bs_select_topk(const bs_dims *dims, const bs_head_cfg *cfg, const int3
  *     unit form one thread-block cluster and merge through distributed shared memory;
  *     split j takes pages [j*p, (j+1)*p), p = ceil(pages / S);
  *   - workspace mode (the rest): each unit's splits are sized by its own page count,
- *     p = max(4 * ceil(pages / 128), m) pages per split (m = 32, or 4 when
+ *     p = max(4 * ceil(pages / 128), m) pages per split (m = 24, or 4 when
  *     max_gather_pages_per_unit > 1024), so at most 32 splits; partials go through the
- *     workspace and the last split to finish merges them.
+ *     workspace and the last split to finish merges them. In the fused step
+ *     (bs_decode_step) only the splits that can hold pages take part: at most
+ *     ceil(min(n_blk, |forced| + k_total) * block_tokens / 16 / m) when m = 24 (the
+ *     others leave at once; the merge is the same, as their records were empty).
  * A unit's plan depends on its own sizes only, so a sub-batch launched with the same S
  * gives bitwise the same per-unit results as the full batch.
  * workspace: device scratch of at least bs_workspace_size(dims) bytes, 16-byte
