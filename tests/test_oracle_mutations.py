@@ -158,6 +158,13 @@ def _decode_step_ed_dma_ignored(wl, step, state, units=None, group_reduce="max",
     return ORIG["decode_step"](wl, step, state, units, group_reduce, attend_units)
 
 
+def _select_forced_within_budget(cls, T, g, sink_tokens, local_tokens, k, k_e, scores=None, evict=None,
+                                 alive=None):
+    """The budget read as including the forced blocks: top_(k - |F|) of the candidates."""
+    kk = max(0, k - len(O.forced_blocks(T, g, sink_tokens, local_tokens)))
+    return ORIG["select_unit"](cls, T, g, sink_tokens, local_tokens, kk, min(k_e, kk), scores, evict, alive)
+
+
 def _decode_step_variant(drop: str):
     """decode_step with one piece of its carried state left out: 'alive' (the eviction
     mask is not carried), 'prev_sel' (the previous selection is not recorded) or 'kbar'
@@ -212,6 +219,7 @@ MUTATIONS = {
     "attention_lse_no_max": ("sparse_attention", _attention_lse_no_max),
     "select_no_eviction": ("select_unit", _select_no_eviction),
     "select_gamma_q_overlaps_gamma_e": ("select_unit", _select_gq_overlaps),
+    "select_forced_within_budget": ("select_unit", _select_forced_within_budget),
     "setdiff_swapped": ("setdiff", _setdiff_swapped),
     "update_wrong_sub_block": ("update_sub_block", _update_wrong_sub_block),
     "swap_no_free": ("block_swap", _swap_no_free),

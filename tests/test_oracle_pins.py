@@ -532,12 +532,40 @@ def check_p13_ed_dma(orc):
             assert np.abs(ed[u].o - plain[u].o).max() > 1e-6
 
 
+def check_p14_selection_size(orc):
+    """S = F + top_k(C) with F and C disjoint ("Technisches Resümee: NOSA", Dual-Selection-
+    Mechanismus; "Technische Samenvatting: Fluxion", Granularity-Budget Selector): a
+    retrieval unit selects |F| + min(k, |C|) blocks, a dual unit |F| + |Gamma_e| +
+    |Gamma_q|; neither exceeds min(n_blk, |F| + k), the bound by which the fused step's
+    workspace attention sizes its splits. |F| also equals the closed form that bound uses,
+    n_sink + n_blk - max(local_lo, n_sink)."""
+    rng = np.random.default_rng(14)
+    for _ in range(300):
+        g = int(rng.choice([4, 8, 16]))
+        T = int(rng.integers(1, 400))
+        sink, local, k = int(rng.integers(0, 3 * g)), int(rng.integers(1, 4 * g)), int(rng.integers(0, 30))
+        n_blk = -(-T // g)
+        F, C = orc.forced_blocks(T, g, sink, local), orc.candidate_blocks(T, g, sink, local)
+        n_sink, local_lo = min(-(-sink // g), n_blk), max(0, T - local) // g
+        assert len(F) == n_sink + n_blk - max(local_lo, n_sink)
+        scores = rng.standard_normal(n_blk)
+        r = orc.select_unit(orc.RETRIEVAL, T, g, sink, local, k, 0, scores)
+        assert len(r.sel) == len(F) + min(k, len(C))
+        assert len(r.sel) <= min(n_blk, len(F) + k)
+        k_e = int(rng.integers(0, k + 1))
+        alive = (rng.random(n_blk) < 0.7).astype(np.uint8)
+        d = orc.select_unit(orc.DUAL, T, g, sink, local, k, k_e, scores, rng.standard_normal(n_blk), alive)
+        n_e = min(k_e, sum(1 for c in C if alive[c]))
+        assert len(d.sel) == len(F) + n_e + min(k - k_e, len(C) - n_e)
+        assert len(d.sel) <= min(n_blk, len(F) + k)
+
+
 ALL_CHECKS = [check_golden_pooling, check_golden_select_retrieval, check_golden_select_dual,
               check_golden_attention, check_p1_full_budget_is_dense, check_p2_streaming_is_sink_window,
               check_p3_select_brute_force, check_p4_p5_eviction, check_p6_pooling_special_cases,
               check_p7_setdiff, check_p8_planted, check_p9_lse_merge, check_p10_incremental,
               check_golden_block_swap, check_p11_block_swap_invariants, check_p12_decode_step_carry,
-              check_golden_ed_dma, check_p13_ed_dma]
+              check_golden_ed_dma, check_p13_ed_dma, check_p14_selection_size]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
